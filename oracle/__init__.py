@@ -1,0 +1,193 @@
+"""Float64 CPU oracle for batch-invariant RMSNorm — TEST INFRASTRUCTURE ONLY.
+
+Only the test suite, ``__graft_entry__.smoke()`` and the benchmark's CPU
+baseline may import this package. The CUDA library never calls it and shares
+no code with it; the product path fails loudly when its CUDA extension is
+missing instead of falling back to anything here.
+
+The arithmetic lives in ``rmsnorm_oracle.c`` (plain C, IEEE double). This module
+only marshals numpy arrays into it. All arrays are float64, C-contiguous,
+row-major ``[T, D]`` for activations, ``[D]`` for the weight and ``[T]`` for the
+inverse RMS. Callers convert bf16 tensors to float64 exactly before calling.
+
+``rounded=True`` applies the method's rounding points (fp32 inverse RMS and
+weight gradient, fp32 zero-centred offset, bf16 round-to-nearest-even outputs);
+the returned values then lie exactly on those grids. ``rounded=False`` is the
+unrounded mathematical function, used by finite-difference pins.
+
+``eps`` is an fp32 argument of the library, so in rounded mode it is first
+rounded to fp32; in unrounded mode it is used as given.
+
+Sources (short keys used in the C file):
+  [Megatron]  Megatron-LM pull request 6859, "Fix the batch-invariant RMSNorm
+              forward and its input gradient"
+  [ZC-norm]   RL-Kernel pull request 467, "[WS1][CUDA][Qwen3-Next] C1:
+              zero-centred RMSNorm references and CUDA kernel"
+  [Residual]  RL-Kernel pull request 414, "[DSv4][P1-5] rmsnorm_residual"
+
+Every function here has a finite-difference, closed-form or brute-force pin
+in ``tests/test_oracle_pins.py``.
+"""
+from __future__ import annotations
+
+import ctypes
+import threading
+
+import numpy as np
+
+from . import build as _build
+
+__all__ = [
+    "round_bf16", "num_threads",
+    "rmsnorm_fwd", "rmsnorm_bwd", "residual_fwd", "residual_bwd",
+    "gated_fwd", "gated_bwd", "weight_grad",
+]
+
+_lock = threading.Lock()
+_lib = None
+
+_D = ctypes.POINTER(ctypes.c_double)
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(_build.build())
+            lib.orc_num_threads.restype = _INT
+            lib.orc_round_bf16.restype = ctypes.c_double
+            lib.orc_round_bf16.argtypes = [ctypes.c_double]
+            lib.orc_rmsnorm_fwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
+            lib.orc_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D]
+            lib.orc_gated_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
+            lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D]
+            lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D]
+            for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_gated_fwd", "orc_gated_bwd",
+                      "orc_weight_grad"):
+                getattr(lib, f).restype = None
+            _lib = lib
+    return _lib
+
+
+def _arr(a, shape=None) -> np.ndarray:
+    a = np.ascontiguousarray(np.asarray(a, dtype=np.float64))
+    if shape is not None and a.shape != tuple(shape):
+        raise ValueError(f"expected shape {tuple(shape)}, got {a.shape}")
+    return a
+
+
+def _p(a):
+    return None if a is None else a.ctypes.data_as(_D)
+
+
+def _eps(eps: float, rounded: bool) -> float:
+    return float(np.float32(eps)) if rounded else float(eps)
+
+
+def num_threads() -> int:
+    """Threads the oracle's parallel loops use (1 if built without OpenMP)."""
+    return int(_load().orc_num_threads())
+
+
+def round_bf16(v) -> np.ndarray:
+    """Round float64 values to bf16 (nearest, ties to even) in one step; returns float64."""
+    lib = _load()
+    v = np.asarray(v, dtype=np.float64)
+    return np.vectorize(lib.orc_round_bf16, otypes=[np.float64])(v) if v.size else v.copy()
+
+
+def rmsnorm_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+    """Plain / zero-centred forward. Returns ``(y [T,D], rstd [T])``."""
+    x = _arr(x)
+    T, D = x.shape
+    w = _arr(w, (D,))
+    y = np.empty((T, D))
+    rstd = np.empty((T,))
+    _load().orc_rmsnorm_fwd(T, D, _p(x), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
+                            int(rounded), _p(y), _p(rstd))
+    return y, rstd
+
+
+def rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma: bool = False, g_res=None,
+                rounded: bool = True):
+    """Plain / zero-centred backward (``g_res`` adds the residual branch's gradient).
+
+    ``rstd`` is the forward's saved inverse RMS. Returns ``(dx [T,D], dgamma [D])``.
+    """
+    x = _arr(x)
+    T, D = x.shape
+    g = _arr(g, (T, D))
+    w = _arr(w, (D,))
+    rstd = _arr(rstd, (T,))
+    gr = None if g_res is None else _arr(g_res, (T, D))
+    dx = np.empty((T, D))
+    dw = np.empty((D,))
+    _load().orc_rmsnorm_bwd(T, D, _p(g), _p(x), _p(w), _p(rstd), _p(gr),
+                            int(zero_centered_gamma), int(rounded), _p(dx), _p(dw))
+    return dx, dw
+
+
+def residual_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+    """``rmsnorm_residual`` forward: the normalised output plus a copy of the input.
+
+    The copy is the input itself, unchanged ([Residual], Summary: the op returns
+    the RMS-normalised output and a copy of the original input, not
+    RMSNorm(x + residual)). Returns ``(y, rstd, x_copy)``.
+    """
+    x = _arr(x)
+    y, rstd = rmsnorm_fwd(x, w, eps, zero_centered_gamma, rounded)
+    return y, rstd, x.copy()
+
+
+def residual_bwd(g, x, w, rstd, g_res, zero_centered_gamma: bool = False, rounded: bool = True):
+    """``rmsnorm_residual`` backward: ``dx`` gains the copy branch's gradient ``g_res``
+    before its single rounding ([Residual], reviewer's "for dx": ``+ d_residual``)."""
+    return rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma, g_res=g_res, rounded=rounded)
+
+
+def gated_fwd(x, z, w, eps: float, zero_centered_gamma: bool = True, rounded: bool = True):
+    """Gated forward ``y = ((x r) w_eff) silu(z)``. Returns ``(y, rstd)``."""
+    x = _arr(x)
+    T, D = x.shape
+    z = _arr(z, (T, D))
+    w = _arr(w, (D,))
+    y = np.empty((T, D))
+    rstd = np.empty((T,))
+    _load().orc_gated_fwd(T, D, _p(x), _p(z), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
+                          int(rounded), _p(y), _p(rstd))
+    return y, rstd
+
+
+def gated_bwd(g, x, z, w, rstd, zero_centered_gamma: bool = True, rounded: bool = True):
+    """Gated backward. Returns ``(dx [T,D], dz [T,D], dw [D])``."""
+    x = _arr(x)
+    T, D = x.shape
+    g = _arr(g, (T, D))
+    z = _arr(z, (T, D))
+    w = _arr(w, (D,))
+    rstd = _arr(rstd, (T,))
+    dx = np.empty((T, D))
+    dz = np.empty((T, D))
+    dw = np.empty((D,))
+    _load().orc_gated_bwd(T, D, _p(g), _p(x), _p(z), _p(w), _p(rstd), int(zero_centered_gamma),
+                          int(rounded), _p(dx), _p(dz), _p(dw))
+    return dx, dz, dw
+
+
+def weight_grad(g, x, rstd, z=None, rounded: bool = True):
+    """Weight gradient alone, ``sum_t g_tj [silu(z_tj)] x_tj r_t`` per column.
+
+    Columns are independent, so this may be called on any subset of columns
+    (with all T rows) to check sampled columns of a large problem; pass the
+    gate ``z`` for the gated variant. Returns ``[D]``.
+    """
+    x = _arr(x)
+    T, D = x.shape
+    g = _arr(g, (T, D))
+    rstd = _arr(rstd, (T,))
+    zz = None if z is None else _arr(z, (T, D))
+    dw = np.empty((D,))
+    _load().orc_weight_grad(T, D, _p(g), _p(zz), _p(x), _p(rstd), int(rounded), _p(dw))
+    return dw

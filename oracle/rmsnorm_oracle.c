@@ -1,0 +1,204 @@
+/*
+ * Float64 CPU oracle for batch-invariant RMSNorm (forward and backward).
+ *
+ * TEST INFRASTRUCTURE ONLY. Nothing on the product path may include, link or
+ * call this file: only the test suite, the smoke check and the benchmark's CPU
+ * baseline use it. It shares no code, header or constant with the CUDA library.
+ *
+ * Sources (cited by the short key in brackets):
+ *   [Megatron]  Megatron-LM pull request 6859, "Fix the batch-invariant RMSNorm
+ *               forward and its input gradient"
+ *   [ZC-norm]   RL-Kernel pull request 467, "[WS1][CUDA][Qwen3-Next] C1: zero-centred
+ *               RMSNorm references and CUDA kernel"
+ *   [Residual]  RL-Kernel pull request 414, "[DSv4][P1-5] rmsnorm_residual"
+ *
+ * Everything is evaluated in IEEE double. Rounding happens only at the points
+ * the method states, and only when `rounded` is non-zero:
+ *   - the saved inverse RMS is an fp32 value                  ([Residual], Implementation)
+ *   - the zero-centred offset is an fp32 add after the fp32 cast
+ *                                     ([Megatron], What does this PR do, item 1;
+ *                                      [ZC-norm], the GemmaRMSNorm forward_native note)
+ *   - activations and activation gradients are bf16, rounded to nearest even
+ *                                                             ([Residual], Implementation)
+ *   - the weight gradient is an fp32 value                    ([Residual], Implementation)
+ * With `rounded == 0` nothing is rounded: that mode is the plain mathematical
+ * function, used by the finite-difference checks.
+ *
+ * Arrays are dense row-major: activations [T][D], weights [D], inverse RMS [T].
+ * Sums run over the index in ascending order with one double accumulator.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+int orc_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+/* Round a double to the nearest bf16 value (8 significant bits, fp32 exponent
+ * range), ties to even, in ONE rounding step from the double. Returns the
+ * rounded value as a double (exactly representable). */
+double orc_round_bf16(double v) {
+    if (isnan(v)) return v;
+    if (isinf(v)) return v;
+    double a = fabs(v);
+    if (a == 0.0) return v;
+    int E;
+    (void)frexp(a, &E);               /* a = m * 2^E, m in [0.5, 1) */
+    int e = E - 1;                    /* a in [2^e, 2^(e+1)) */
+    int q = (e < -126) ? -133 : e - 7; /* quantum exponent: normal 2^(e-7), subnormal 2^-133 */
+    double n = ldexp(a, -q);          /* exact scaling by a power of two */
+    double nr = nearbyint(n);         /* default mode: round half to even */
+    double r = ldexp(nr, q);
+    /* Overflow: anything that rounds to 2^128 or beyond is infinite in bf16. */
+    if (r >= ldexp(1.0, 128)) r = INFINITY;
+    return signbit(v) ? -r : r;
+}
+
+/* Round a double to fp32 (C conversion, round to nearest even). */
+static double fl32(double v) { return (double)(float)v; }
+
+static double maybe_bf16(double v, int rounded) { return rounded ? orc_round_bf16(v) : v; }
+static double maybe_fl32(double v, int rounded) { return rounded ? fl32(v) : v; }
+
+/* Effective weight: w, or w + 1 applied in fp32 after the fp32 cast when the
+ * gamma is zero-centred ([Megatron], What does this PR do, item 1). */
+static double w_eff(double w, int zero_centered, int rounded) {
+    if (!zero_centered) return w;
+    return maybe_fl32(w + 1.0, rounded);
+}
+
+/* Inverse RMS of one row: r = (mean_j x_j^2 + eps)^(-1/2), mean = (sum x^2) / D
+ * ([Megatron], What does this PR do, item 2, definition of r; [Residual], the
+ * reviewer's "Forward" summary). */
+static double row_inv_rms(const double* x, int64_t D, double eps) {
+    double ss = 0.0;
+    for (int64_t j = 0; j < D; ++j) ss += x[j] * x[j];
+    double mean = ss / (double)D;
+    return 1.0 / sqrt(mean + eps);
+}
+
+/* silu(z) = z * sigmoid(z), sigmoid(z) = 1 / (1 + exp(-z)). */
+static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
+static double silu(double z) { return z * sigmoid(z); }
+
+/* ------------------------------------------------------------------------ */
+/* Plain / zero-centred forward:  y = (x * r) * w_eff,  rstd = r              */
+/* ([Megatron], item 1; [Residual], reviewer's "Forward" summary)            */
+/* ------------------------------------------------------------------------ */
+void orc_rmsnorm_fwd(int64_t T, int64_t D, const double* x, const double* w, double eps,
+                     int zero_centered, int rounded, double* y, double* rstd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* xr = x + t * D;
+        double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);
+        rstd[t] = r;
+        for (int64_t j = 0; j < D; ++j)
+            y[t * D + j] = maybe_bf16(xr[j] * r * w_eff(w[j], zero_centered, rounded), rounded);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Weight gradient: dgamma_j = sum_t g_tj * x_tj * r_t  (ascending t)         */
+/* ([Megatron], item 2, g_w unchanged; [Residual], reviewer's "for dgamma")  */
+/* Gated variant (z != NULL): g is replaced by g * silu(z), the gradient that */
+/* reaches the normalised-and-scaled value.                                   */
+/* Columns are independent: any column subset may be passed with all T rows.  */
+/* ------------------------------------------------------------------------ */
+void orc_weight_grad(int64_t T, int64_t D, const double* g, const double* z,
+                     const double* x, const double* r, int rounded, double* dw) {
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < D; ++j) {
+        double acc = 0.0;
+        for (int64_t t = 0; t < T; ++t) {
+            double gt = g[t * D + j];
+            if (z) gt *= silu(z[t * D + j]);
+            acc += gt * x[t * D + j] * r[t];
+        }
+        dw[j] = maybe_fl32(acc, rounded);
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Plain / zero-centred / residual backward.                                  */
+/*   s    = sum_i g_i x_i w_eff_i                                             */
+/*   dx_k = g_k w_eff_k r - (r^3 x_k / D) * s  [+ g_res_k]                    */
+/* ([Megatron], item 2, the dL/dx_k formula; [Residual], reviewer's "for dx", */
+/* which adds d_residual)                                                     */
+/* `rstd` is the forward's saved value; `g_res` may be NULL (zero).           */
+/* ------------------------------------------------------------------------ */
+void orc_rmsnorm_bwd(int64_t T, int64_t D, const double* g, const double* x, const double* w,
+                     const double* rstd, const double* g_res, int zero_centered, int rounded,
+                     double* dx, double* dw) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* gr = g + t * D;
+        const double* xr = x + t * D;
+        double r = rstd[t];
+        double s = 0.0;
+        for (int64_t i = 0; i < D; ++i) s += gr[i] * xr[i] * w_eff(w[i], zero_centered, rounded);
+        for (int64_t k = 0; k < D; ++k) {
+            double v = gr[k] * w_eff(w[k], zero_centered, rounded) * r - (r * r * r * xr[k] / (double)D) * s;
+            if (g_res) v += g_res[t * D + k];
+            dx[t * D + k] = maybe_bf16(v, rounded);
+        }
+    }
+    orc_weight_grad(T, D, g, NULL, x, rstd, rounded, dw);
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gated forward (Qwen3-Next, vLLM convention: weight multiply in fp32):      */
+/*   u = (x * r) * w_eff,  y = u * silu(z)                                    */
+/* ([ZC-norm], the two gated-norm conventions: Qwen3NextRMSNormGatedOp)      */
+/* ------------------------------------------------------------------------ */
+void orc_gated_fwd(int64_t T, int64_t D, const double* x, const double* z, const double* w,
+                   double eps, int zero_centered, int rounded, double* y, double* rstd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* xr = x + t * D;
+        double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);
+        rstd[t] = r;
+        for (int64_t j = 0; j < D; ++j) {
+            double u = xr[j] * r * w_eff(w[j], zero_centered, rounded);
+            y[t * D + j] = maybe_bf16(u * silu(z[t * D + j]), rounded);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------ */
+/* Gated backward. With q = silu(z) and u = x r w_eff (so y = u q):           */
+/*   dL/du = g q, which enters the plain backward in place of g:              */
+/*     s    = sum_i (g_i q_i) x_i w_eff_i                                     */
+/*     dx_k = (g_k q_k) w_eff_k r - (r^3 x_k / D) * s                         */
+/*   dz_k = g_k u_k silu'(z_k),  silu'(z) = sig(z) (1 + z (1 - sig(z)))       */
+/*   dw_j = sum_t g_tj q_tj x_tj r_t                                          */
+/* ------------------------------------------------------------------------ */
+void orc_gated_bwd(int64_t T, int64_t D, const double* g, const double* x, const double* z,
+                   const double* w, const double* rstd, int zero_centered, int rounded,
+                   double* dx, double* dz, double* dw) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* gr = g + t * D;
+        const double* xr = x + t * D;
+        const double* zr = z + t * D;
+        double r = rstd[t];
+        double s = 0.0;
+        for (int64_t i = 0; i < D; ++i) s += gr[i] * silu(zr[i]) * xr[i] * w_eff(w[i], zero_centered, rounded);
+        for (int64_t k = 0; k < D; ++k) {
+            double we = w_eff(w[k], zero_centered, rounded);
+            double v = gr[k] * silu(zr[k]) * we * r - (r * r * r * xr[k] / (double)D) * s;
+            dx[t * D + k] = maybe_bf16(v, rounded);
+            double sg = sigmoid(zr[k]);
+            double u = xr[k] * r * we;
+            dz[t * D + k] = maybe_bf16(gr[k] * u * (sg * (1.0 + zr[k] * (1.0 - sg))), rounded);
+        }
+    }
+    orc_weight_grad(T, D, g, z, x, rstd, rounded, dw);
+}
