@@ -1,0 +1,148 @@
+/*
+ * rmsnorm.h — C ABI of the GB300 (sm_103a) batch-invariant RMSNorm library.
+ *
+ * Operations (sources, cited by page title and section):
+ *   [Megatron]  Megatron-LM pull request 6859, "Fix the batch-invariant RMSNorm
+ *               forward and its input gradient" — "What does this PR do", items 1-2.
+ *   [ZC-norm]   RL-Kernel pull request 467, "[WS1][CUDA][Qwen3-Next] C1: zero-centred
+ *               RMSNorm references and CUDA kernel" — the GemmaRMSNorm forward_native
+ *               note (+1 in fp32) and the two gated-norm conventions.
+ *   [Residual]  RL-Kernel pull request 414, "[DSv4][P1-5] rmsnorm_residual" —
+ *               Summary, Implementation, and the reviewer's Forward/Backward notes.
+ *
+ * Forward, per row t of x [T][D]:
+ *   r_t   = rsqrt( (sum_j x_tj^2) / D + eps )          saved as fp32 rstd[t]
+ *   w_eff = w, or (fp32) w + 1.0f when zero_centered_gamma is set
+ *   y_tj  = bf16( (x_tj * r_t) * w_eff_j )             two separately rounded fp32 multiplies
+ * Backward, per row (g = dL/dy, saved r):
+ *   s     = sum_i g_i x_i w_eff_i
+ *   dx_k  = bf16( g_k w_eff_k r  -  (r^3 x_k / D) * s  [+ g_res_k] )
+ *   dgamma_j = sum_t g_tj x_tj r_t                     fp32
+ *
+ * Batch invariance: every row is reduced by a fixed tree whose shape depends on
+ * D alone, so y[t], rstd[t] and dx[t] are bitwise independent of T, of the row's
+ * position, of the other rows and of the GPU's SM count. dgamma is a sum over
+ * rows; it is computed with no atomics, in fixed-size row chunks (pass 1) whose
+ * partial sums are added in a fixed order (pass 2), so it is bitwise identical
+ * from run to run and across GPUs with different SM counts.
+ *
+ * Common conventions for every entry point:
+ *   - Activations (x, z, g, g_res, y, dx, dz, x_copy) are bf16, row-major [T][D]
+ *     with a row stride `ld*` in ELEMENTS (ld >= D). They are passed as raw bf16
+ *     bit patterns (rmsn_bf16). w / dgamma are fp32 [D]; rstd is fp32 [T].
+ *   - All pointers are DEVICE pointers, 16-byte aligned; every ld* is a multiple
+ *     of 8 (so each row starts on a 16-byte boundary). D is a multiple of 8 with
+ *     8 <= D <= 16384. eps is finite and >= 0. 0 <= T < 2^31; T == 0 returns
+ *     RMSN_OK without launching anything.
+ *   - Outputs must not overlap inputs or each other.
+ *   - The library allocates nothing. Scratch for the weight gradient is the
+ *     caller's workspace `ws` of at least rmsnorm_bwd_workspace_bytes(T, D) bytes
+ *     (16-byte aligned). The caller owns every buffer.
+ *   - Work is enqueued asynchronously on `stream` (NULL = legacy default stream);
+ *     calls on one stream execute in order. A call that returns an error has
+ *     enqueued nothing.
+ *   - Validation runs on the host before any launch; invalid arguments are
+ *     rejected with a status code. There is no fallback path of any kind.
+ *   - Launch failures are reported as RMSN_ECUDA (from cudaGetLastError). Faults
+ *     during execution surface on the stream as CUDA errors, as usual.
+ *   - Each kernel bounds every wait on its asynchronous copies; if a wait ever
+ *     exceeds its limit the kernel stops, records a flag readable with
+ *     rmsnorm_device_error(), and returns.
+ */
+#ifndef RMSNORM_GB300_H_
+#define RMSNORM_GB300_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef uint16_t rmsn_bf16;               /* raw bf16 bit pattern                      */
+typedef struct CUstream_st* rmsn_stream;  /* identical to cudaStream_t; NULL = default */
+
+enum rmsn_status {
+    RMSN_OK = 0,
+    RMSN_EINVAL = -1,        /* null pointer, bad size, ld < D, negative/non-finite eps */
+    RMSN_EALIGN = -2,        /* a pointer or row stride is not 16-byte aligned          */
+    RMSN_EUNSUPPORTED = -3,  /* D outside [8, 16384] or not a multiple of 8             */
+    RMSN_ECUDA = -4,         /* a CUDA runtime or driver call failed                    */
+    RMSN_EWORKSPACE = -5     /* workspace missing or smaller than the query's answer    */
+};
+
+/* Human-readable name of a status code (static string). */
+const char* rmsnorm_status_string(int status);
+
+/* Forward, plain or zero-centred ([Megatron] item 1; [Residual] Forward).
+ *   x [T][ldx] in, w [D] in, y [T][ldy] out, rstd [T] out (fp32 inverse RMS). */
+int rmsnorm_fwd(const rmsn_bf16* x, int64_t ldx, const float* w,
+                rmsn_bf16* y, int64_t ldy, float* rstd,
+                int64_t T, int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream);
+
+/* Bytes of workspace the backward entry points need for T rows of width D
+ * (0 for T == 0; also 0 for an unsupported D). */
+size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t D);
+
+/* Backward, plain or zero-centred ([Megatron] item 2; [Residual] Backward).
+ *   g [T][ldg] (dL/dy) in, x [T][ldx] in, w [D] in, rstd [T] in (the forward's),
+ *   dx [T][lddx] out, dgamma [D] out (fp32), ws workspace.
+ *   If dgamma is NULL, only pass 1 runs: the per-chunk partial sums are left in
+ *   ws and rmsnorm_dgamma_reduce() finishes them later. */
+int rmsnorm_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                const float* w, const float* rstd,
+                rmsn_bf16* dx, int64_t lddx, float* dgamma,
+                void* ws, size_t ws_bytes,
+                int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
+/* rmsnorm_residual forward ([Residual] Summary): the plain forward, plus a
+ * bitwise copy of x into x_copy [T][ldxc]. It is not RMSNorm(x + residual). */
+int rmsnorm_residual_fwd(const rmsn_bf16* x, int64_t ldx, const float* w,
+                         rmsn_bf16* y, int64_t ldy, float* rstd,
+                         rmsn_bf16* x_copy, int64_t ldxc,
+                         int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                         rmsn_stream stream);
+
+/* rmsnorm_residual backward ([Residual] Backward: dx gains d_residual).
+ *   g_res [T][ldgr] is the gradient arriving at x_copy, added in fp32 before dx's
+ *   single bf16 rounding; NULL means zero. Other arguments as rmsnorm_bwd. */
+int rmsnorm_residual_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                         const float* w, const float* rstd,
+                         const rmsn_bf16* g_res, int64_t ldgr,
+                         rmsn_bf16* dx, int64_t lddx, float* dgamma,
+                         void* ws, size_t ws_bytes,
+                         int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
+/* Gated forward, Qwen3-Next / vLLM convention ([ZC-norm], gated-norm conventions):
+ *   y = bf16( ((x * r) * w_eff) * silu(z) ), weight multiply and gate in fp32,
+ *   silu(z) = z * (1 / (1 + expf(-z))).  z [T][ldz] in (the gate). */
+int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz,
+                      const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
+                      int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                      rmsn_stream stream);
+
+/* Gated backward: with q = silu(z) and u = (x r) w_eff,
+ *   dx = plain backward with g*q in place of g;  dz = bf16( g u silu'(z) );
+ *   dw_j = sum_t g q x r. dw NULL: as rmsnorm_bwd with dgamma NULL. */
+int rmsnorm_gated_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                      const rmsn_bf16* z, int64_t ldz, const float* w, const float* rstd,
+                      rmsn_bf16* dx, int64_t lddx, rmsn_bf16* dz, int64_t lddz, float* dw,
+                      void* ws, size_t ws_bytes,
+                      int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
+/* Weight-gradient pass 2 on its own: sums the per-chunk partials that a backward
+ * call with a NULL dgamma/dw left in ws (same T, D and workspace), in the fixed
+ * order, into dgamma [D]. ws must be unchanged since that call. */
+int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                          float* dgamma, rmsn_stream stream);
+
+/* Reads the device-side error flags of the current device (OR of all kernels'
+ * flags since the last clear) into *flags; clears them if `clear` is non-zero.
+ * Synchronises with the device. 0 means no kernel ever gave up on a wait. */
+int rmsnorm_device_error(unsigned int* flags, int clear);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* RMSNORM_GB300_H_ */

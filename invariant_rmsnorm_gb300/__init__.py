@@ -1,0 +1,236 @@
+"""Python binding of the GB300 batch-invariant RMSNorm library (C ABI in
+``include/rmsnorm.h``).
+
+Argument marshalling only: every function here takes torch tensors that the
+caller allocated on a CUDA device, checks dtypes/shapes/devices, and passes raw
+pointers, row strides and sizes to the ``extern "C"`` entry point of the same
+name in ``_build/librmsnorm_gb300.so``. All arithmetic runs in the library's
+sm_103a kernels. If the library has not been built, ``load()`` raises; there is
+no other implementation to fall back to.
+
+Activations are bf16 ``[T, D]`` with unit column stride (any row stride that
+is a multiple of 8 elements); weights and weight gradients fp32 ``[D]``;
+inverse RMS fp32 ``[T]``. Work is enqueued on ``stream`` (default: the current
+torch stream of the tensors' device).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+from typing import Optional
+
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "load", "lib_path", "RmsNormError", "workspace_bytes",
+    "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
+    "rmsnorm_gated_fwd", "rmsnorm_gated_bwd", "rmsnorm_dgamma_reduce",
+    "rmsnorm_bwd_workspace_bytes", "rmsnorm_status_string", "rmsnorm_device_error",
+    "EXPORTED_SYMBOLS",
+]
+
+EXPORTED_SYMBOLS = (
+    "rmsnorm_status_string", "rmsnorm_fwd", "rmsnorm_bwd_workspace_bytes", "rmsnorm_bwd",
+    "rmsnorm_residual_fwd", "rmsnorm_residual_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
+    "rmsnorm_dgamma_reduce", "rmsnorm_device_error",
+)
+
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_INT = ctypes.c_int
+_F = ctypes.c_float
+_SZ = ctypes.c_size_t
+
+_SIGS = {
+    "rmsnorm_status_string": (ctypes.c_char_p, [_INT]),
+    "rmsnorm_fwd": (_INT, [_P, _I64, _P, _P, _I64, _P, _I64, _I64, _F, _INT, _P]),
+    "rmsnorm_bwd_workspace_bytes": (_SZ, [_I64, _I64]),
+    "rmsnorm_bwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _P, _SZ, _I64, _I64, _INT, _P]),
+    "rmsnorm_residual_fwd": (_INT, [_P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _F, _INT, _P]),
+    "rmsnorm_residual_bwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _SZ,
+                                    _I64, _I64, _INT, _P]),
+    "rmsnorm_gated_fwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _F, _INT, _P]),
+    "rmsnorm_gated_bwd": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P,
+                                 _SZ, _I64, _I64, _INT, _P]),
+    "rmsnorm_dgamma_reduce": (_INT, [_P, _SZ, _I64, _I64, _P, _P]),
+    "rmsnorm_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
+}
+
+_lock = threading.Lock()
+_lib: Optional[ctypes.CDLL] = None
+
+
+class RmsNormError(RuntimeError):
+    """A non-zero status returned by the library."""
+
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn}: {rmsnorm_status_string(status)} (status {status})")
+
+
+def lib_path() -> str:
+    return _build.lib_path()
+
+
+def load(path: Optional[str] = None) -> ctypes.CDLL:
+    """Load the shared library (once). Raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            p = path or lib_path()
+            if not os.path.exists(p):
+                raise RuntimeError(
+                    f"CUDA library not built ({p} missing): run `python -c \"import __graft_entry__ as g; "
+                    f"g.build()\"` first. There is no non-CUDA implementation.")
+            lib = ctypes.CDLL(p)
+            for name, (res, args) in _SIGS.items():
+                fn = getattr(lib, name)
+                fn.restype = res
+                fn.argtypes = args
+            _lib = lib
+    return _lib
+
+
+# --------------------------------------------------------------------------
+# marshalling helpers
+# --------------------------------------------------------------------------
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _act(t: torch.Tensor, name: str, T: int, D: int) -> int:
+    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2:
+        raise TypeError(f"{name}: expected a 2-D bf16 CUDA tensor, got {t.dtype} {t.device} {tuple(t.shape)}")
+    if tuple(t.shape) != (T, D):
+        raise ValueError(f"{name}: expected shape {(T, D)}, got {tuple(t.shape)}")
+    if D > 1 and t.stride(1) != 1:
+        raise ValueError(f"{name}: columns must be contiguous")
+    return t.stride(0) if T > 1 else max(t.stride(0), D)
+
+
+def _f32(t: torch.Tensor, name: str, n: int):
+    if t.dtype != torch.float32 or not t.is_cuda or t.dim() != 1 or t.shape[0] != n or (n > 1 and t.stride(0) != 1):
+        raise TypeError(f"{name}: expected a contiguous fp32 CUDA tensor of shape ({n},)")
+
+
+def _stream(stream, dev) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream(dev)
+    return ctypes.c_void_p(stream.cuda_stream if isinstance(stream, torch.cuda.Stream) else int(stream))
+
+
+def _check(fn: str, status: int):
+    if status != 0:
+        raise RmsNormError(fn, status)
+
+
+def _ws(ws: torch.Tensor):
+    if not ws.is_cuda:
+        raise TypeError("ws: expected a CUDA tensor")
+    return ctypes.c_void_p(ws.data_ptr()), ws.numel() * ws.element_size()
+
+
+# --------------------------------------------------------------------------
+# entry points (same names as the C ABI)
+# --------------------------------------------------------------------------
+def rmsnorm_status_string(status: int) -> str:
+    return load().rmsnorm_status_string(int(status)).decode()
+
+
+def rmsnorm_bwd_workspace_bytes(T: int, D: int) -> int:
+    return int(load().rmsnorm_bwd_workspace_bytes(int(T), int(D)))
+
+
+workspace_bytes = rmsnorm_bwd_workspace_bytes
+
+
+def rmsnorm_fwd(x, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: bool = False, stream=None):
+    T, D = x.shape
+    ldx, ldy = _act(x, "x", T, D), _act(y, "y", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_fwd", load().rmsnorm_fwd(_ptr(x), ldx, _ptr(w), _ptr(y), ldy, _ptr(rstd), T, D,
+                                             float(eps), int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_residual_fwd(x, w, y, rstd, x_copy, eps: float = 1e-6, zero_centered_gamma: bool = False,
+                         stream=None):
+    T, D = x.shape
+    ldx, ldy, ldc = _act(x, "x", T, D), _act(y, "y", T, D), _act(x_copy, "x_copy", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_residual_fwd", load().rmsnorm_residual_fwd(
+        _ptr(x), ldx, _ptr(w), _ptr(y), ldy, _ptr(rstd), _ptr(x_copy), ldc, T, D, float(eps),
+        int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_fwd(x, z, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: bool = True, stream=None):
+    T, D = x.shape
+    ldx, ldz, ldy = _act(x, "x", T, D), _act(z, "z", T, D), _act(y, "y", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_gated_fwd", load().rmsnorm_gated_fwd(
+        _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(y), ldy, _ptr(rstd), T, D, float(eps),
+        int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_bwd(g, x, w, rstd, dx, dgamma, ws, zero_centered_gamma: bool = False, stream=None):
+    """``dgamma`` may be None: pass 1 only (partials stay in ``ws``)."""
+    T, D = x.shape
+    ldg, ldx, lddx = _act(g, "g", T, D), _act(x, "x", T, D), _act(dx, "dx", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_bwd", load().rmsnorm_bwd(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dgamma), wp, wb, T, D,
+        int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_residual_bwd(g, x, w, rstd, g_res, dx, dgamma, ws, zero_centered_gamma: bool = False,
+                         stream=None):
+    """``g_res`` may be None (zero); ``dgamma`` may be None (pass 1 only)."""
+    T, D = x.shape
+    ldg, ldx, lddx = _act(g, "g", T, D), _act(x, "x", T, D), _act(dx, "dx", T, D)
+    ldgr = _act(g_res, "g_res", T, D) if g_res is not None else D
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_residual_bwd", load().rmsnorm_residual_bwd(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dx), lddx, _ptr(dgamma),
+        wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_bwd(g, x, z, w, rstd, dx, dz, dw, ws, zero_centered_gamma: bool = True, stream=None):
+    """``dw`` may be None (pass 1 only)."""
+    T, D = x.shape
+    ldg, ldx, ldz = _act(g, "g", T, D), _act(x, "x", T, D), _act(z, "z", T, D)
+    lddx, lddz = _act(dx, "dx", T, D), _act(dz, "dz", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dw is not None:
+        _f32(dw, "dw", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_gated_bwd", load().rmsnorm_gated_bwd(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dz), lddz,
+        _ptr(dw), wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_dgamma_reduce(ws, T: int, D: int, dgamma, stream=None):
+    _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_dgamma_reduce", load().rmsnorm_dgamma_reduce(
+        wp, wb, int(T), int(D), _ptr(dgamma), _stream(stream, dgamma.device)))
+
+
+def rmsnorm_device_error(clear: bool = True) -> int:
+    """Device-side error flags since the last clear (0 = none). Synchronises."""
+    flags = ctypes.c_uint(0)
+    _check("rmsnorm_device_error", load().rmsnorm_device_error(ctypes.byref(flags), int(clear)))
+    return int(flags.value)

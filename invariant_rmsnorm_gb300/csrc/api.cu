@@ -1,0 +1,305 @@
+// C-ABI layer: argument validation, row-shape selection, device caches and
+// dispatch to the kernel launchers. Every check runs on the host before any
+// launch; there is no fallback path.
+#include <cmath>
+#include <cstring>
+#include <map>
+#include <mutex>
+#include <tuple>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace rmsn {
+
+// ---------------------------------------------------------------------------
+// Row shape: a pure function of D (this is what makes a row's reduction tree,
+// and therefore its bits, independent of everything but D).
+// ---------------------------------------------------------------------------
+RowCfg row_cfg(int D) {
+    RowCfg c{};
+    const int NV = D / 8;  // 16-byte vectors per row
+    const int ntmax = NV > 1024 ? 512 : 256;
+    const int need = (NV + ntmax - 1) / ntmax;
+    c.narrow = false;
+    c.vpt = need <= 1 ? 1 : (need <= 2 ? 2 : 4);
+    c.threads = ((NV + c.vpt - 1) / c.vpt + 31) / 32 * 32;
+    c.group = 0;
+    c.rows_per_stage = 1;
+    c.chunk_rows = kWideChunkRows;
+    return c;
+}
+
+int64_t num_chunks(int64_t T, int D) {
+    const int64_t c = row_cfg(D).chunk_rows;
+    return (T + c - 1) / c;
+}
+
+// ---------------------------------------------------------------------------
+// Per-device caches
+// ---------------------------------------------------------------------------
+namespace {
+std::mutex g_mu;
+std::map<int, int> g_sms;
+std::map<std::tuple<int, const void*>, int> g_smem_set;
+std::map<std::tuple<int, const void*, int, int>, int> g_occ;
+
+int current_device() {
+    int d = 0;
+    cudaGetDevice(&d);
+    return d;
+}
+}  // namespace
+
+int sm_count() {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto it = g_sms.find(dev);
+    if (it != g_sms.end()) return it->second;
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) n = 1;
+    g_sms[dev] = n;
+    return n;
+}
+
+cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(dev, kernel);
+    auto it = g_smem_set.find(key);
+    if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
+    cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e == cudaSuccess) g_smem_set[key] = bytes;
+    return e;
+}
+
+int ctas_per_sm(const void* kernel, int threads, int smem_bytes) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(dev, kernel, threads, smem_bytes);
+    auto it = g_occ.find(key);
+    if (it != g_occ.end()) return it->second;
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes) != cudaSuccess) n = 0;
+    g_occ[key] = n;
+    return n;
+}
+
+}  // namespace rmsn
+
+using namespace rmsn;
+
+// ---------------------------------------------------------------------------
+// Validation helpers
+// ---------------------------------------------------------------------------
+namespace {
+
+inline bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int check_shape(int64_t T, int64_t D) {
+    if (T < 0 || T >= (int64_t(1) << 31)) return RMSN_EINVAL;
+    if (D < 8 || D > kMaxD || (D % 8) != 0) return RMSN_EUNSUPPORTED;
+    return RMSN_OK;
+}
+
+// An activation matrix [T][ld] of bf16 (required = must be non-null).
+int check_act(const void* p, int64_t ld, int64_t D) {
+    if (p == nullptr) return RMSN_EINVAL;
+    if (ld < D || ld > (int64_t(1) << 40)) return RMSN_EINVAL;
+    if (!aligned16(p) || (ld % 8) != 0) return RMSN_EALIGN;
+    return RMSN_OK;
+}
+
+int check_vec(const void* p) {
+    if (p == nullptr) return RMSN_EINVAL;
+    if (!aligned16(p)) return RMSN_EALIGN;
+    return RMSN_OK;
+}
+
+int check_eps(float eps) { return (std::isfinite(eps) && eps >= 0.0f) ? RMSN_OK : RMSN_EINVAL; }
+
+int check_ws(const void* ws, size_t ws_bytes, int64_t T, int64_t D) {
+    const size_t need = static_cast<size_t>(num_chunks(T, static_cast<int>(D))) * static_cast<size_t>(D) * 4u;
+    if (ws == nullptr || ws_bytes < need) return RMSN_EWORKSPACE;
+    if (!aligned16(ws)) return RMSN_EALIGN;
+    return RMSN_OK;
+}
+
+#define RMSN_TRY(expr)                  \
+    do {                                \
+        const int _st = (expr);         \
+        if (_st != RMSN_OK) return _st; \
+    } while (0)
+
+inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ECUDA; }
+
+int run_fwd(Mode m, const FwdArgs& a, cudaStream_t s) {
+    const RowCfg c = row_cfg(a.D);
+    const cudaError_t e = c.narrow ? launch_narrow_fwd(m, a, c, s) : launch_wide_fwd(m, a, c, s);
+    return cuda_status(e);
+}
+
+int run_bwd(Mode m, const BwdArgs& a, float* dgamma, cudaStream_t s) {
+    const RowCfg c = row_cfg(a.D);
+    cudaError_t e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);
+    if (e != cudaSuccess) return RMSN_ECUDA;
+    if (dgamma != nullptr) e = launch_dgamma_reduce(a.partials, num_chunks(a.T, a.D), a.D, dgamma, s);
+    return cuda_status(e);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// Entry points
+// ---------------------------------------------------------------------------
+extern "C" {
+
+const char* rmsnorm_status_string(int status) {
+    switch (status) {
+        case RMSN_OK: return "RMSN_OK";
+        case RMSN_EINVAL: return "RMSN_EINVAL: invalid argument (null pointer, size, stride or eps)";
+        case RMSN_EALIGN: return "RMSN_EALIGN: pointer or row stride not 16-byte aligned";
+        case RMSN_EUNSUPPORTED: return "RMSN_EUNSUPPORTED: D must be a multiple of 8 in [8, 16384]";
+        case RMSN_ECUDA: return "RMSN_ECUDA: a CUDA call failed";
+        case RMSN_EWORKSPACE: return "RMSN_EWORKSPACE: workspace missing or too small";
+        default: return "unknown rmsnorm status";
+    }
+}
+
+size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t D) {
+    if (check_shape(T, D) != RMSN_OK || T == 0) return 0;
+    return static_cast<size_t>(num_chunks(T, static_cast<int>(D))) * static_cast<size_t>(D) * 4u;
+}
+
+int rmsnorm_fwd(const rmsn_bf16* x, int64_t ldx, const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
+                int64_t T, int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kPlain, a, stream);
+}
+
+int rmsnorm_residual_fwd(const rmsn_bf16* x, int64_t ldx, const float* w, rmsn_bf16* y, int64_t ldy,
+                         float* rstd, rmsn_bf16* x_copy, int64_t ldxc, int64_t T, int64_t D, float eps,
+                         int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_act(x_copy, ldxc, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd; a.xc = x_copy; a.ldxc = ldxc;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kResidual, a, stream);
+}
+
+int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz, const float* w,
+                      rmsn_bf16* y, int64_t ldy, float* rstd, int64_t T, int64_t D, float eps,
+                      int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kGated, a, stream);
+}
+
+int rmsnorm_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
+                const float* rstd, rmsn_bf16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes,
+                int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.w = w; a.rstd = rstd; a.dx = dx; a.lddx = lddx;
+    a.partials = static_cast<float*>(ws); a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(kPlain, a, dgamma, stream);
+}
+
+int rmsnorm_residual_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
+                         const float* rstd, const rmsn_bf16* g_res, int64_t ldgr, rmsn_bf16* dx, int64_t lddx,
+                         float* dgamma, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                         int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    // A zero residual gradient is the plain backward.
+    return run_bwd(g_res ? kResidual : kPlain, a, dgamma, stream);
+}
+
+int rmsnorm_gated_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z,
+                      int64_t ldz, const float* w, const float* rstd, rmsn_bf16* dx, int64_t lddx, rmsn_bf16* dz,
+                      int64_t lddz, float* dw, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                      int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_act(dz, lddz, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dw) RMSN_TRY(check_vec(dw));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.dz = dz; a.lddz = lddz; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(kGated, a, dw, stream);
+}
+
+int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D, float* dgamma,
+                          rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    return cuda_status(launch_dgamma_reduce(static_cast<const float*>(ws), num_chunks(T, static_cast<int>(D)),
+                                            static_cast<int>(D), dgamma, stream));
+}
+
+int rmsnorm_device_error(unsigned int* flags, int clear) {
+    if (flags == nullptr) return RMSN_EINVAL;
+    *flags = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e == cudaSuccess) e = wide_read_error(flags, clear != 0);
+    if (e == cudaSuccess) e = narrow_read_error(flags, clear != 0);
+    return cuda_status(e);
+}
+
+}  // extern "C"

@@ -1,0 +1,189 @@
+// Shared device-side building blocks for the sm_103a RMSNorm kernels:
+// inline-PTX wrappers for mbarriers, bulk (TMA) copies and cp.async, bf16
+// packing, separately rounded fp32 arithmetic, and the fixed butterfly sum.
+//
+// Every wait on an mbarrier is bounded: a waiter that sees no progress for
+// kWaitTimeoutNs of global time gives up and reports failure, and the kernels
+// turn that into an error flag plus a clean exit (no trap, no endless spin).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "rmsnorm.h"
+
+namespace rmsn {
+
+// ---------------------------------------------------------------------------
+// Constants that fix the numerics. They depend on nothing but D, never on T,
+// the row index, the grid or the GPU's SM count.
+// ---------------------------------------------------------------------------
+constexpr int kWideChunkRows = 32;       // weight-gradient chunk (rows), wide path
+constexpr int kNarrowThreads = 256;      // narrow path CTA size
+constexpr int kNarrowChunkRowsMin = 64;  // weight-gradient chunk (rows), narrow path
+constexpr int kMaxD = 16384;
+constexpr int kReduceWarps = 16;         // weight-gradient pass 2: warps per 32 columns
+
+// Device-side error codes (bit flags OR-ed into the library's error words).
+constexpr unsigned kErrWaitTimeout = 1u;
+
+constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ unsigned long long global_timer_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count) : "memory");
+}
+
+// Make mbarrier initialisation visible to the async (TMA) proxy.
+__device__ __forceinline__ void fence_mbar_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+// Order earlier generic-proxy shared-memory accesses (made visible to this
+// thread by a barrier) before its later async-proxy (TMA) writes.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// Arrive once and add `bytes` to the transaction count of the current phase.
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
+                 ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Bounded wait for the phase with parity `parity` to complete. Returns false if
+// kWaitTimeoutNs of global time elapsed without completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    uint32_t done = 0;
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(addr), "r"(parity) : "memory");
+        if (done) return true;
+        if ((it & 255u) == 0u) {
+            const unsigned long long now = global_timer_ns();
+            if (it == 0) t0 = now;
+            else if (now - t0 > kWaitTimeoutNs) return false;
+        }
+    }
+}
+
+// 1-D bulk copy global -> shared, completion counted on `bar` (bytes).
+// dst and src 16-byte aligned; bytes a multiple of 16.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes, uint64_t* bar,
+                                         uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cta.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
+// 2-D tiled tensor copy global -> shared (box described by the tensor map).
+// c0 = innermost (column) coordinate, c1 = row coordinate.
+__device__ __forceinline__ void tensor2d_g2s(void* dst, const CUtensorMap* map, int c0, int c1,
+                                             uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2, %3}], [%4], %5;"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(c1), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
+// 1-D tiled tensor copy global -> shared.
+__device__ __forceinline__ void tensor1d_g2s(void* dst, const CUtensorMap* map, int c0, uint64_t* bar,
+                                             uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.tensor.1d.shared::cta.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1, {%2}], [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(map), "r"(c0), "r"(smem_u32(bar)), "l"(policy) : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
+}
+
+// 4-byte asynchronous copy global -> shared whose completion is signalled on
+// `bar` by a no-increment arrive (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async4_arrive(void* dst, const void* src, uint64_t* bar) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// L2 policy for streamed data read once.
+__device__ __forceinline__ uint64_t policy_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 128-bit streaming global store.
+__device__ __forceinline__ void st_global_cs(void* p, uint4 v) {
+    asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
+                 ::"l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ uint4 ld_shared_v4(const void* p) {
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(smem_u32(p)) : "memory");
+    return v;
+}
+
+// ---------------------------------------------------------------------------
+// bf16 <-> fp32 (exact widening; round-to-nearest-even narrowing)
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void unpack8(const uint4 v, float f[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        f[2 * i] = __uint_as_float(w[i] << 16);
+        f[2 * i + 1] = __uint_as_float(w[i] & 0xffff0000u);
+    }
+}
+
+__device__ __forceinline__ uint4 pack8(const float f[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __nv_bfloat162 h = __floats2bfloat162_rn(f[2 * i], f[2 * i + 1]);  // .x = low half
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// ---------------------------------------------------------------------------
+// Separately rounded fp32 arithmetic (never contracted into FMA).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b); }
+__device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
+__device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
+
+// sigmoid(z) = 1 / (1 + exp(-z)) in fp32 (CUDA expf, IEEE division).
+__device__ __forceinline__ float sigmoidf_rn(float z) { return __fdiv_rn(1.0f, fadd(1.0f, expf(-z))); }
+
+// Butterfly sum over aligned groups of WIDTH lanes (a power of two <= 32).
+// Every lane of a group ends with the same bits (IEEE addition commutes).
+template <int WIDTH>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = WIDTH / 2; o > 0; o >>= 1) v = fadd(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+
+}  // namespace rmsn

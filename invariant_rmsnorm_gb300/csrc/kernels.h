@@ -1,0 +1,74 @@
+// Internal launch interface between the C-ABI layer (api.cu) and the kernel
+// translation units. Not part of the public ABI.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace rmsn {
+
+enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2 };
+
+// Everything a forward launch needs (unused pointers are null).
+struct FwdArgs {
+    const uint16_t* x; int64_t ldx;
+    const uint16_t* z; int64_t ldz;     // gate (gated)
+    const float* w;
+    uint16_t* y; int64_t ldy;
+    float* rstd;
+    uint16_t* xc; int64_t ldxc;         // input copy (residual)
+    int64_t T; int D; float eps; int zc;
+};
+
+// Everything a backward (pass 1) launch needs.
+struct BwdArgs {
+    const uint16_t* g; int64_t ldg;
+    const uint16_t* x; int64_t ldx;
+    const uint16_t* z; int64_t ldz;     // gate (gated)
+    const uint16_t* gres; int64_t ldgr; // gradient of the input copy (residual)
+    const float* w;
+    const float* rstd;
+    uint16_t* dx; int64_t lddx;
+    uint16_t* dz; int64_t lddz;         // gated
+    float* partials;                    // [nchunks][D] fp32 (workspace)
+    int64_t T; int D; int zc;
+};
+
+// Row-shape configuration: a pure function of D.
+struct RowCfg {
+    bool narrow;         // D <= 256: several rows per CTA, one lane group per row
+    int threads;         // CTA size
+    int vpt;             // 16-byte vectors per thread per row (wide); 1 (narrow)
+    int group;           // lanes per row (narrow), a power of two <= 32
+    int rows_per_stage;  // rows per pipeline stage (narrow); 1 (wide)
+    int chunk_rows;      // rows per weight-gradient partial
+};
+
+RowCfg row_cfg(int D);
+int64_t num_chunks(int64_t T, int D);
+
+// Launchers (return the launch's cudaError_t; arguments already validated).
+cudaError_t launch_wide_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_wide_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_narrow_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_narrow_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_dgamma_reduce(const float* partials, int64_t nchunks, int D, float* out,
+                                 cudaStream_t s);
+
+// Device properties, cached per device.
+int sm_count();
+cudaError_t ensure_smem_attr(const void* kernel, int bytes);
+int ctas_per_sm(const void* kernel, int threads, int smem_bytes);
+
+// Error-word access for each kernel translation unit.
+cudaError_t wide_read_error(unsigned* flags, bool clear);
+cudaError_t narrow_read_error(unsigned* flags, bool clear);
+
+// Tensor-map encoding through the driver entry point (no libcuda link needed).
+// Rows of bf16: box = [box_rows][D]. Vector of fp32: box = [box].
+cudaError_t encode_rows_2d(CUtensorMap* map, const void* base, int64_t T, int D, int64_t ld_elems,
+                           int box_rows);
+cudaError_t encode_vec_1d(CUtensorMap* map, const float* base, int64_t T, int box);
+
+}  // namespace rmsn

@@ -60,10 +60,11 @@ def _load():
             lib.orc_round_bf16.restype = ctypes.c_double
             lib.orc_round_bf16.argtypes = [ctypes.c_double]
             lib.orc_rmsnorm_fwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
-            lib.orc_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D]
+            lib.orc_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D, _D, _D]
             lib.orc_gated_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
-            lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D]
-            lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D]
+            lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
+                                          _D, _D, _D, _D, _D]
+            lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D, _D]
             for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_gated_fwd", "orc_gated_bwd",
                       "orc_weight_grad"):
                 getattr(lib, f).restype = None
@@ -111,10 +112,13 @@ def rmsnorm_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bo
 
 
 def rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma: bool = False, g_res=None,
-                rounded: bool = True):
+                rounded: bool = True, diagnostics: bool = False):
     """Plain / zero-centred backward (``g_res`` adds the residual branch's gradient).
 
-    ``rstd`` is the forward's saved inverse RMS. Returns ``(dx [T,D], dgamma [D])``.
+    ``rstd`` is the forward's saved inverse RMS. Returns ``(dx [T,D], dgamma [D])``,
+    plus, with ``diagnostics``, a dict with ``dx_pre`` (dx before its bf16
+    rounding), ``dx_scale`` (magnitude of dx's terms before cancellation) and
+    ``dw_abs`` (sum of |terms| of each weight-gradient column).
     """
     x = _arr(x)
     T, D = x.shape
@@ -124,9 +128,12 @@ def rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma: bool = False, g_res=None,
     gr = None if g_res is None else _arr(g_res, (T, D))
     dx = np.empty((T, D))
     dw = np.empty((D,))
+    diag = {k: np.empty(s) for k, s in (("dx_pre", (T, D)), ("dx_scale", (T, D)), ("dw_abs", (D,)))} \
+        if diagnostics else {}
     _load().orc_rmsnorm_bwd(T, D, _p(g), _p(x), _p(w), _p(rstd), _p(gr),
-                            int(zero_centered_gamma), int(rounded), _p(dx), _p(dw))
-    return dx, dw
+                            int(zero_centered_gamma), int(rounded), _p(dx), _p(dw),
+                            _p(diag.get("dx_pre")), _p(diag.get("dx_scale")), _p(diag.get("dw_abs")))
+    return (dx, dw, diag) if diagnostics else (dx, dw)
 
 
 def residual_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
@@ -141,10 +148,12 @@ def residual_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: b
     return y, rstd, x.copy()
 
 
-def residual_bwd(g, x, w, rstd, g_res, zero_centered_gamma: bool = False, rounded: bool = True):
+def residual_bwd(g, x, w, rstd, g_res, zero_centered_gamma: bool = False, rounded: bool = True,
+                 diagnostics: bool = False):
     """``rmsnorm_residual`` backward: ``dx`` gains the copy branch's gradient ``g_res``
     before its single rounding ([Residual], reviewer's "for dx": ``+ d_residual``)."""
-    return rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma, g_res=g_res, rounded=rounded)
+    return rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma, g_res=g_res, rounded=rounded,
+                       diagnostics=diagnostics)
 
 
 def gated_fwd(x, z, w, eps: float, zero_centered_gamma: bool = True, rounded: bool = True):
@@ -160,8 +169,11 @@ def gated_fwd(x, z, w, eps: float, zero_centered_gamma: bool = True, rounded: bo
     return y, rstd
 
 
-def gated_bwd(g, x, z, w, rstd, zero_centered_gamma: bool = True, rounded: bool = True):
-    """Gated backward. Returns ``(dx [T,D], dz [T,D], dw [D])``."""
+def gated_bwd(g, x, z, w, rstd, zero_centered_gamma: bool = True, rounded: bool = True,
+              diagnostics: bool = False):
+    """Gated backward. Returns ``(dx [T,D], dz [T,D], dw [D])``, plus with
+    ``diagnostics`` a dict as in ``rmsnorm_bwd`` with ``dz_pre`` and ``dz_scale``
+    (|g u| sig (1 + |z| (1 - sig))) added."""
     x = _arr(x)
     T, D = x.shape
     g = _arr(g, (T, D))
@@ -171,17 +183,22 @@ def gated_bwd(g, x, z, w, rstd, zero_centered_gamma: bool = True, rounded: bool 
     dx = np.empty((T, D))
     dz = np.empty((T, D))
     dw = np.empty((D,))
+    names = (("dx_pre", (T, D)), ("dx_scale", (T, D)), ("dz_pre", (T, D)), ("dz_scale", (T, D)),
+             ("dw_abs", (D,)))
+    diag = {k: np.empty(s) for k, s in names} if diagnostics else {}
     _load().orc_gated_bwd(T, D, _p(g), _p(x), _p(z), _p(w), _p(rstd), int(zero_centered_gamma),
-                          int(rounded), _p(dx), _p(dz), _p(dw))
-    return dx, dz, dw
+                          int(rounded), _p(dx), _p(dz), _p(dw),
+                          *[_p(diag.get(k)) for k, _ in names])
+    return (dx, dz, dw, diag) if diagnostics else (dx, dz, dw)
 
 
-def weight_grad(g, x, rstd, z=None, rounded: bool = True):
+def weight_grad(g, x, rstd, z=None, rounded: bool = True, with_abs: bool = False):
     """Weight gradient alone, ``sum_t g_tj [silu(z_tj)] x_tj r_t`` per column.
 
     Columns are independent, so this may be called on any subset of columns
     (with all T rows) to check sampled columns of a large problem; pass the
-    gate ``z`` for the gated variant. Returns ``[D]``.
+    gate ``z`` for the gated variant. Returns ``[D]`` (and, with ``with_abs``,
+    the per-column sum of |terms| as a second array).
     """
     x = _arr(x)
     T, D = x.shape
@@ -189,5 +206,6 @@ def weight_grad(g, x, rstd, z=None, rounded: bool = True):
     rstd = _arr(rstd, (T,))
     zz = None if z is None else _arr(z, (T, D))
     dw = np.empty((D,))
-    _load().orc_weight_grad(T, D, _p(g), _p(zz), _p(x), _p(rstd), int(rounded), _p(dw))
-    return dw
+    dwa = np.empty((D,)) if with_abs else None
+    _load().orc_weight_grad(T, D, _p(g), _p(zz), _p(x), _p(rstd), int(rounded), _p(dw), _p(dwa))
+    return (dw, dwa) if with_abs else dw

@@ -111,18 +111,23 @@ void orc_rmsnorm_fwd(int64_t T, int64_t D, const double* x, const double* w, dou
 /* Gated variant (z != NULL): g is replaced by g * silu(z), the gradient that */
 /* reaches the normalised-and-scaled value.                                   */
 /* Columns are independent: any column subset may be passed with all T rows.  */
+/* dw_abs (may be NULL) receives sum_t |term|, the scale of the rounding     */
+/* error any finite-precision evaluation of the sum can make.                */
 /* ------------------------------------------------------------------------ */
 void orc_weight_grad(int64_t T, int64_t D, const double* g, const double* z,
-                     const double* x, const double* r, int rounded, double* dw) {
+                     const double* x, const double* r, int rounded, double* dw, double* dw_abs) {
 #pragma omp parallel for schedule(static)
     for (int64_t j = 0; j < D; ++j) {
-        double acc = 0.0;
+        double acc = 0.0, mag = 0.0;
         for (int64_t t = 0; t < T; ++t) {
             double gt = g[t * D + j];
             if (z) gt *= silu(z[t * D + j]);
-            acc += gt * x[t * D + j] * r[t];
+            double term = gt * x[t * D + j] * r[t];
+            acc += term;
+            mag += fabs(term);
         }
         dw[j] = maybe_fl32(acc, rounded);
+        if (dw_abs) dw_abs[j] = mag;
     }
 }
 
@@ -133,24 +138,37 @@ void orc_weight_grad(int64_t T, int64_t D, const double* g, const double* z,
 /* ([Megatron], item 2, the dL/dx_k formula; [Residual], reviewer's "for dx", */
 /* which adds d_residual)                                                     */
 /* `rstd` is the forward's saved value; `g_res` may be NULL (zero).           */
+/* Optional diagnostics (each may be NULL): dx_pre = dx before its bf16       */
+/* rounding; dx_scale = |g_k w_k r| + (r^3 |x_k| / D) sum_i |g_i x_i w_i|     */
+/* [+ |g_res_k|], the magnitude the terms of dx_k had before they cancelled;  */
+/* dw_abs as in orc_weight_grad.                                              */
 /* ------------------------------------------------------------------------ */
 void orc_rmsnorm_bwd(int64_t T, int64_t D, const double* g, const double* x, const double* w,
                      const double* rstd, const double* g_res, int zero_centered, int rounded,
-                     double* dx, double* dw) {
+                     double* dx, double* dw, double* dx_pre, double* dx_scale, double* dw_abs) {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         const double* gr = g + t * D;
         const double* xr = x + t * D;
         double r = rstd[t];
-        double s = 0.0;
-        for (int64_t i = 0; i < D; ++i) s += gr[i] * xr[i] * w_eff(w[i], zero_centered, rounded);
+        double s = 0.0, s_abs = 0.0;
+        for (int64_t i = 0; i < D; ++i) {
+            double term = gr[i] * xr[i] * w_eff(w[i], zero_centered, rounded);
+            s += term;
+            s_abs += fabs(term);
+        }
         for (int64_t k = 0; k < D; ++k) {
-            double v = gr[k] * w_eff(w[k], zero_centered, rounded) * r - (r * r * r * xr[k] / (double)D) * s;
-            if (g_res) v += g_res[t * D + k];
+            double a = gr[k] * w_eff(w[k], zero_centered, rounded) * r;
+            double b = (r * r * r * xr[k] / (double)D) * s;
+            double v = a - b;
+            double mag = fabs(a) + (r * r * r * fabs(xr[k]) / (double)D) * s_abs;
+            if (g_res) { v += g_res[t * D + k]; mag += fabs(g_res[t * D + k]); }
             dx[t * D + k] = maybe_bf16(v, rounded);
+            if (dx_pre) dx_pre[t * D + k] = v;
+            if (dx_scale) dx_scale[t * D + k] = mag;
         }
     }
-    orc_weight_grad(T, D, g, NULL, x, rstd, rounded, dw);
+    orc_weight_grad(T, D, g, NULL, x, rstd, rounded, dw, dw_abs);
 }
 
 /* ------------------------------------------------------------------------ */
@@ -182,23 +200,35 @@ void orc_gated_fwd(int64_t T, int64_t D, const double* x, const double* z, const
 /* ------------------------------------------------------------------------ */
 void orc_gated_bwd(int64_t T, int64_t D, const double* g, const double* x, const double* z,
                    const double* w, const double* rstd, int zero_centered, int rounded,
-                   double* dx, double* dz, double* dw) {
+                   double* dx, double* dz, double* dw,
+                   double* dx_pre, double* dx_scale, double* dz_pre, double* dz_scale, double* dw_abs) {
+    /* Diagnostics as in orc_rmsnorm_bwd; dz_scale = |g u| sig (1 + |z| (1 - sig)). */
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         const double* gr = g + t * D;
         const double* xr = x + t * D;
         const double* zr = z + t * D;
         double r = rstd[t];
-        double s = 0.0;
-        for (int64_t i = 0; i < D; ++i) s += gr[i] * silu(zr[i]) * xr[i] * w_eff(w[i], zero_centered, rounded);
+        double s = 0.0, s_abs = 0.0;
+        for (int64_t i = 0; i < D; ++i) {
+            double term = gr[i] * silu(zr[i]) * xr[i] * w_eff(w[i], zero_centered, rounded);
+            s += term;
+            s_abs += fabs(term);
+        }
         for (int64_t k = 0; k < D; ++k) {
             double we = w_eff(w[k], zero_centered, rounded);
-            double v = gr[k] * silu(zr[k]) * we * r - (r * r * r * xr[k] / (double)D) * s;
+            double a = gr[k] * silu(zr[k]) * we * r;
+            double v = a - (r * r * r * xr[k] / (double)D) * s;
             dx[t * D + k] = maybe_bf16(v, rounded);
+            if (dx_pre) dx_pre[t * D + k] = v;
+            if (dx_scale) dx_scale[t * D + k] = fabs(a) + (r * r * r * fabs(xr[k]) / (double)D) * s_abs;
             double sg = sigmoid(zr[k]);
             double u = xr[k] * r * we;
-            dz[t * D + k] = maybe_bf16(gr[k] * u * (sg * (1.0 + zr[k] * (1.0 - sg))), rounded);
+            double d = gr[k] * u * (sg * (1.0 + zr[k] * (1.0 - sg)));
+            dz[t * D + k] = maybe_bf16(d, rounded);
+            if (dz_pre) dz_pre[t * D + k] = d;
+            if (dz_scale) dz_scale[t * D + k] = fabs(gr[k] * u) * (sg * (1.0 + fabs(zr[k]) * (1.0 - sg)));
         }
     }
-    orc_weight_grad(T, D, g, z, x, rstd, rounded, dw);
+    orc_weight_grad(T, D, g, z, x, rstd, rounded, dw, dw_abs);
 }

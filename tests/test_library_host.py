@@ -1,0 +1,102 @@
+"""Host-side checks of the C-ABI library (no GPU needed, no compute calls).
+
+The library must load on a machine without a GPU, export every entry point
+that include/rmsnorm.h declares, answer the workspace query, and reject
+invalid arguments on the host, before touching the CUDA runtime.
+"""
+from __future__ import annotations
+
+import ctypes
+import glob
+import os
+import re
+
+import pytest
+
+import invariant_rmsnorm_gb300 as rn
+from invariant_rmsnorm_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return rn.load()
+
+
+def _declared():
+    names = set()
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = open(h).read()
+        txt = re.sub(r"/\*.*?\*/", "", txt, flags=re.S)
+        names |= set(re.findall(r"\b(rmsnorm_\w+)\s*\(", txt))
+    return names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    declared = _declared()
+    assert declared, "no declarations found in include/*.h"
+    assert declared == set(rn.EXPORTED_SYMBOLS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for st in (0, -1, -2, -3, -4, -5):
+        assert rn.rmsnorm_status_string(st).startswith("RMSN_")
+    assert "unknown" in rn.rmsnorm_status_string(17)
+
+
+@pytest.mark.parametrize("T,D", [(1, 128), (16, 128), (32768, 4096), (262144, 128), (131072, 7168), (33, 8)])
+def test_workspace_query(lib, T, D):
+    b = rn.rmsnorm_bwd_workspace_bytes(T, D)
+    assert b > 0 and b % (4 * D) == 0
+    assert b // (4 * D) < T + 64  # at most one partial row per chunk
+    assert rn.rmsnorm_bwd_workspace_bytes(0, D) == 0
+    assert rn.rmsnorm_bwd_workspace_bytes(T, 7) == 0
+
+
+def _fwd(lib, x=16, ldx=128, w=16, y=16, ldy=128, r=16, T=4, D=128, eps=1e-6):
+    return lib.rmsnorm_fwd(ctypes.c_void_p(x), ldx, ctypes.c_void_p(w), ctypes.c_void_p(y), ldy,
+                           ctypes.c_void_p(r), T, D, eps, 0, None)
+
+
+def test_host_validation_rejects_before_launch(lib):
+    # Fake, never-dereferenced addresses: every case fails validation first.
+    A = 1 << 20
+    assert _fwd(lib, x=A, y=A, w=A, r=A, D=7) == -3          # D not a multiple of 8
+    assert _fwd(lib, x=A, y=A, w=A, r=A, D=16392, ldx=16392, ldy=16392) == -3  # D too large
+    assert _fwd(lib, x=0, y=A, w=A, r=A) == -1               # null input
+    assert _fwd(lib, x=A + 2, y=A, w=A, r=A) == -2           # misaligned pointer
+    assert _fwd(lib, x=A, y=A, w=A, r=A, ldx=132) == -2      # row stride not 16-byte aligned
+    assert _fwd(lib, x=A, y=A, w=A, r=A, ldx=120) == -1      # ld < D
+    assert _fwd(lib, x=A, y=A, w=A, r=A, eps=-1.0) == -1     # negative eps
+    assert _fwd(lib, x=A, y=A, w=A, r=A, eps=float("nan")) == -1
+    assert _fwd(lib, x=A, y=A, w=A, r=A, T=-1) == -1
+    assert _fwd(lib, x=0, y=0, w=0, r=0, T=0) == 0           # empty: OK, nothing launched
+    # backward: missing / short workspace
+    need = rn.rmsnorm_bwd_workspace_bytes(4, 128)
+    st = lib.rmsnorm_bwd(A, 128, A, 128, A, A, A, 128, A, None, need, 4, 128, 0, None)
+    assert st == -5
+    st = lib.rmsnorm_bwd(A, 128, A, 128, A, A, A, 128, A, A, need - 4, 4, 128, 0, None)
+    assert st == -5
+    st = lib.rmsnorm_gated_bwd(A, 128, A, 128, 0, 128, A, A, A, 128, A, 128, A, A, need, 4, 128, 1, None)
+    assert st == -1
+    st = lib.rmsnorm_dgamma_reduce(A, need - 1, 4, 128, A, None)
+    assert st == -5
+    assert lib.rmsnorm_device_error(None, 0) == -1
+
+
+def test_package_has_no_non_cuda_path():
+    """The binding refuses to run without the built library (no fallback)."""
+    import importlib
+    src = open(os.path.join(ROOT, "invariant_rmsnorm_gb300", "__init__.py")).read()
+    assert "oracle" not in src and "import numpy" not in src
+    mod = importlib.import_module("invariant_rmsnorm_gb300")
+    with pytest.raises(RuntimeError):
+        mod._lib, saved = None, mod._lib
+        try:
+            mod.load(path=os.path.join(ROOT, "does-not-exist.so"))
+        finally:
+            mod._lib = saved
