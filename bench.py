@@ -1,0 +1,439 @@
+"""Benchmark: batch-invariant RMSNorm fwd+bwd on GB300, reported as achieved HBM GB/s.
+
+Workload (one step): rmsnorm_residual forward + backward at T=32768 rows,
+D=4096, bf16 activations, fp32 gamma ~1+N(0,0.05), x/g/g_res ~N(0,1), eps=1e-6
+— the configuration the metric is quoted on (the residual op's published
+benchmark shape, RL-Kernel pull request 414 "[DSv4][P1-5] rmsnorm_residual",
+Benchmarks). A step is three launches on one stream: the forward, backward
+pass 1 (dx plus weight-gradient chunk partials) and pass 2 (fixed-order sum).
+
+value = algorithmic bytes of the step (14*D + 8 bytes per row: x read, y and
+x_copy written, rstd written; g, x, g_res and rstd read, dx written) / device
+time of the step, summed over ranks (each rank runs its own replica: rows are
+independent, so N GPUs process N batches with no exchange). Inputs are 1.9 GB
+per step, far larger than the 129 MB L2, so no flush is needed between steps.
+
+--impl reference times the float64 CPU oracle (the only reference: the pages
+hold no runnable code) on bounded row samples of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+T_ROWS, D_COLS, EPS = 32768, 4096, 1e-6
+METRIC = "RMSNorm fwd+bwd HBM GB/s (% of GB300 peak) at T=32768, D=4096, bf16"
+PAGES_H100_CUDA_MS = 10.043916  # residual fwd+bwd, T=32768, D=4096, H100 PCIe (context only)
+
+
+def step_bytes(T, D):
+    return T * (14 * D + 8)
+
+
+def bwd_pass1_bytes(T, D):
+    return T * (8 * D + 4)
+
+
+def fwd_bytes(T, D):
+    return T * (6 * D + 4)
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def source_hash():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "invariant_rmsnorm_gb300", "csrc")
+    for name in sorted(os.listdir(csrc)):
+        with open(os.path.join(csrc, name), "rb") as f:
+            h.update(name.encode() + f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic():
+    """DRAM bytes per launch of backward pass 1, from the committed ncu summary —
+    only while the kernel sources are the ones that were profiled."""
+    p = os.path.join(ROOT, "profiles", "bwd_residual_T32768_D4096_traffic.json")
+    if not os.path.exists(p):
+        return None
+    with open(p) as f:
+        d = json.load(f)
+    if d.get("source_hash") != source_hash():
+        return None
+    return d.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# clocks sampled during the timed region
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str):
+        self.gpu_id = gpu_id
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", self.gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self._t = threading.Thread(target=self._read, daemon=True)
+            self._t.start()
+        except (OSError, ValueError):
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self._t.join(timeout=2)
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 8:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[4:8]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (one process per GPU; replicas, no data exchange)
+# ---------------------------------------------------------------------------
+def dist_setup(n_gpus):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if torch.cuda.is_available():
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def dist_max(v):
+    import torch
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        t = torch.tensor([float(v)], device="cuda" if torch.cuda.is_available() else "cpu")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        return float(t.item())
+    return float(v)
+
+
+def barrier():
+    import torch.distributed as dist
+    if dist.is_available() and dist.is_initialized():
+        dist.barrier()
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    import invariant_rmsnorm_gb300 as rn
+    from invariant_rmsnorm_gb300 import synth
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    rn.load()
+    T, D = T_ROWS, D_COLS
+    wl = synth.residual(dev, seed=rank)
+    y = torch.empty_like(wl.x)
+    xc = torch.empty_like(wl.x)
+    dx = torch.empty_like(wl.x)
+    rstd = torch.empty(T, device=dev)
+    dg = torch.empty(D, device=dev)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        rn.rmsnorm_residual_fwd(wl.x, wl.w, y, rstd, xc, EPS, False, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        rn.rmsnorm_residual_bwd(wl.g, wl.x, wl.w, rstd, wl.g_res, dx, None, ws, False, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        rn.rmsnorm_dgamma_reduce(ws, T, D, dg, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(args.steps)]
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    gpu_id = "0"
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(dev.index or 0)
+    sampler = ClockSampler(gpu_id)
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)  # let the sampler take its first reading
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs[k])
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    total_ms = dist_max(start.elapsed_time(stop))
+    fwd_ms = sum(e[0].elapsed_time(e[1]) for e in evs) / args.steps
+    bwd_ms = sum(e[1].elapsed_time(e[2]) for e in evs) / args.steps
+    red_ms = sum(e[2].elapsed_time(e[3]) for e in evs) / args.steps
+    ms_per_step = total_ms / args.steps
+    value = world * step_bytes(T, D) / (ms_per_step * 1e-3) / 1e9
+
+    # end to end through the public API: pinned host inputs -> device -> outputs -> host
+    h_in = [t.cpu().pin_memory() for t in (wl.x, wl.g, wl.g_res)]
+    h_w = wl.w.cpu().pin_memory()
+    d_in = [torch.empty_like(t) for t in (wl.x, wl.g, wl.g_res)]
+    d_w = torch.empty_like(wl.w)
+    h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in (y, xc, dx, rstd, dg)]
+    h2d = sum(t.numel() * t.element_size() for t in h_in) + h_w.numel() * 4
+    d2h = sum(t.numel() * t.element_size() for t in h_out)
+
+    def e2e_step():
+        for h, d in zip(h_in, d_in):
+            d.copy_(h, non_blocking=True)
+        d_w.copy_(h_w, non_blocking=True)
+        rn.rmsnorm_residual_fwd(d_in[0], d_w, y, rstd, xc, EPS, False, stream=stream)
+        rn.rmsnorm_residual_bwd(d_in[1], d_in[0], d_w, rstd, d_in[2], dx, dg, ws, False, stream=stream)
+        for h, d in zip(h_out, (y, xc, dx, rstd, dg)):
+            h.copy_(d, non_blocking=True)
+
+    e2e_steps = max(3, min(20, args.steps))
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    barrier()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(e2e_steps):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = dist_max(e0.elapsed_time(e1)) / e2e_steps
+    e2e_value = world * step_bytes(T, D) / (e2e_ms * 1e-3) / 1e9
+
+    # side measurements (not part of `value`): plain and gated fwd+bwd
+    extra = side_measurements(rn, synth, dev, stream) if rank == 0 else {}
+
+    cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    peak, peak_kind = peaks()
+    bwd_gbs = bwd_pass1_bytes(T, D) / (bwd_ms * 1e-3) / 1e9
+    traffic = recorded_traffic()
+    if rank == 0:
+        out = {
+            "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_per_step, 5),
+            "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": round((PAGES_H100_CUDA_MS / ms_per_step) * world, 3),
+            "vs_baseline_basis": "pages' H100 PCIe residual fwd+bwd at the same shape (10.043916 ms); context only",
+            "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "rmsnorm_residual fwd+bwd", "T": T, "D": D, "io": "bf16 activations, fp32 gamma/rstd/dgamma",
+                       "eps": EPS, "zero_centered_gamma": False, "parallelism": f"replicas x{world}",
+                       "l2": "inputs 1.88 GB per step, larger than L2; no flush"},
+            "pct_of_peak": round(100.0 * value / (world * peak), 2),
+            "kernels_ms": {"fwd": round(fwd_ms, 5), "bwd_pass1": round(bwd_ms, 5), "dgamma_pass2": round(red_ms, 5)},
+            "roofline": {"kernel": "wide_bwd_kernel (residual, pass 1)", "bound": "hbm",
+                         "achieved": round(bwd_gbs, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(bwd_gbs / peak, 4), "peak_kind": peak_kind,
+                         "traffic": traffic, "algorithmic_bytes_per_launch": bwd_pass1_bytes(T, D)},
+            "fwd_roofline": {"achieved": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9, 2), "peak": peak,
+                             "frac": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9 / peak, 4)},
+            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4)},
+            "gpu_launches": 3 * args.steps,
+            "clocks": clocks,
+            "cpu_baseline": cpu,
+            "extra": extra,
+        }
+        print(json.dumps(out))
+    barrier()
+
+
+def side_measurements(rn, synth, dev, stream, reps=50):
+    import torch
+    res = {}
+    # plain fwd+bwd, same shape (the metric's literal op): 10*D + 8 bytes per row
+    T, D = T_ROWS, D_COLS
+    wl = synth.tiny_plain(dev, seed=3, T=T, D=D)
+    y, dx = torch.empty_like(wl.x), torch.empty_like(wl.x)
+    r, dg = torch.empty(T, device=dev), torch.empty(D, device=dev)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+
+    def plain():
+        rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, False, stream=stream)
+        rn.rmsnorm_bwd(wl.g, wl.x, wl.w, r, dx, dg, ws, False, stream=stream)
+    res["plain_fwd_bwd_gbs"] = _time_gbs(plain, T * (10 * D + 8), reps, stream)
+    del wl, y, dx
+    # gated, 262144 x 128: 16*D + 8 bytes per row
+    g = synth.gated(dev, seed=4)
+    T, D = g.T, g.D
+    y, dx, dz = torch.empty_like(g.x), torch.empty_like(g.x), torch.empty_like(g.x)
+    r, dw = torch.empty(T, device=dev), torch.empty(D, device=dev)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+
+    def gated():
+        rn.rmsnorm_gated_fwd(g.x, g.z, g.w, y, r, EPS, True, stream=stream)
+        rn.rmsnorm_gated_bwd(g.g, g.x, g.z, g.w, r, dx, dz, dw, ws, True, stream=stream)
+    res["gated_262144x128_fwd_bwd_gbs"] = _time_gbs(gated, T * (16 * D + 8), reps, stream)
+    return res
+
+
+def _time_gbs(fn, nbytes, reps, stream):
+    import torch
+    for _ in range(5):
+        fn()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    torch.cuda.synchronize()
+    a.record(stream)
+    for _ in range(reps):
+        fn()
+    b.record(stream)
+    torch.cuda.synchronize()
+    ms = a.elapsed_time(b) / reps
+    return {"gbs": round(nbytes / (ms * 1e-3) / 1e9, 2), "ms": round(ms, 5)}
+
+
+# ---------------------------------------------------------------------------
+# CPU baseline / reference arm: the float64 oracle, as it stands
+# ---------------------------------------------------------------------------
+def _oracle_sample(rows, seed=0):
+    import numpy as np
+
+    from invariant_rmsnorm_gb300 import synth
+    wl = synth.residual("cpu", seed=seed, T=rows, D=D_COLS)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    return f(wl.x), f(wl.w), f(wl.g), f(wl.g_res)
+
+
+def _oracle_step(arrs):
+    import oracle
+    x, w, g, gr = arrs
+    y, r, xc = oracle.residual_fwd(x, w, EPS, False)
+    oracle.residual_bwd(g, x, w, r, gr, False)
+
+
+def cpu_baseline_sample(target_s=10.0):
+    import oracle
+    rows = 2048
+    arrs = _oracle_sample(rows)
+    _oracle_step(arrs)
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < target_s:
+        _oracle_step(arrs)
+        n += 1
+    dt = time.perf_counter() - t0
+    return {"value": round(n * step_bytes(rows, D_COLS) / dt / 1e9, 4), "unit": "GB/s",
+            "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} repetitions of {rows} rows x {D_COLS} (residual fwd+bwd, float64 C oracle), {dt:.1f} s"}
+
+
+def run_reference(args):
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    if rank != 0:
+        return
+    import oracle
+    # size each step so that warmup + steps take about two minutes at most
+    probe_rows = 64
+    arrs = _oracle_sample(probe_rows, seed=1)
+    t0 = time.perf_counter()
+    _oracle_step(arrs)
+    per_row = (time.perf_counter() - t0) / probe_rows
+    budget = 120.0 / max(1, args.steps + args.warmup)
+    rows = int(max(8, min(4096, budget / max(per_row, 1e-9))))
+    arrs = _oracle_sample(rows, seed=2)
+    for _ in range(args.warmup):
+        _oracle_step(arrs)
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        _oracle_step(arrs)
+    dt = time.perf_counter() - t0
+    value = args.steps * step_bytes(rows, D_COLS) / dt / 1e9
+    out = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": "rmsnorm_residual fwd+bwd", "T": T_ROWS, "D": D_COLS,
+                   "sample_rows_per_step": rows},
+        "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
+                         "sample": f"{rows} of {T_ROWS} rows per step, float64 C oracle"},
+        "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(out))
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed CPU-oracle sample")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.steps < 1:
+        ap.error("--steps must be at least 1")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -98,3 +98,68 @@ def check_bf16_within_1ulp(got: np.ndarray, ref_rounded: np.ndarray):
     ref = np.asarray(ref_rounded, np.float64)
     same_special = (np.isnan(got) & np.isnan(ref)) | (np.isinf(got) & (got == ref))
     return same_special | (np.abs(got - ref) <= bf16_ulp(ref))
+
+
+def _ulp_of_max(a, b):
+    return bf16_ulp(np.maximum(np.abs(a), np.abs(b)))
+
+
+def bf16_parity_mask(got, ref_rounded, pre=None, scale=None, K: float = 96.0):
+    """Parity of a bf16 output with the oracle.
+
+    Clause 1 (the bar): |got - RN(ref)| <= 1 bf16 ulp of RN(ref).
+    Clause 2 (only with ``pre``/``scale``, for outputs whose terms cancel):
+    |got - ref| <= 1/2 ulp + K * 2^-24 * scale, where ``ref`` is the exact
+    pre-rounding value and ``scale`` the magnitude of its terms: the error an
+    fp32 evaluation with at most K separately rounded steps can make, plus the
+    final bf16 rounding. Returns (mask, n_clause2).
+    """
+    got = np.asarray(got, np.float64)
+    m1 = check_bf16_within_1ulp(got, ref_rounded)
+    if pre is None:
+        return m1, 0
+    m2 = np.abs(got - pre) <= 0.5 * _ulp_of_max(got, pre) + K * U32 * scale
+    return m1 | m2, int(np.count_nonzero(m2 & ~m1))
+
+
+def assert_bf16_parity(name, got, ref_rounded, pre=None, scale=None, K: float = 96.0):
+    mask, n2 = bf16_parity_mask(got, ref_rounded, pre, scale, K)
+    bad = np.argwhere(~mask)
+    if bad.size:
+        i = tuple(bad[0])
+        msg = f"{name}: {len(bad)} of {mask.size} outside tolerance; first at {i}: got {got[i]!r} " \
+              f"ref {ref_rounded[i]!r}"
+        if pre is not None:
+            msg += f" pre {pre[i]!r} scale {scale[i]!r}"
+        raise AssertionError(msg)
+    return n2
+
+
+def assert_rel(name, got, ref, rtol):
+    got = np.asarray(got, np.float64)
+    ok = np.abs(got - ref) <= rtol * np.abs(ref)
+    if not ok.all():
+        i = tuple(np.argwhere(~ok)[0])
+        raise AssertionError(f"{name}: {np.count_nonzero(~ok)} outside rtol {rtol}; first at {i}: "
+                             f"got {got[i]!r} ref {ref[i]!r}")
+
+
+def dgamma_bound_gamma(chunk_rows: int, nchunks: int, reduce_warps: int = 16) -> float:
+    """Rounding-error factor of the library's fixed weight-gradient tree: products
+    (2-3 roundings, +8 for a gate), C sequential adds per chunk, ceil(n/16)
+    sequential adds per warp in pass 2, 16 warp totals."""
+    return (chunk_rows + -(-nchunks // reduce_warps) + reduce_warps + 8) * U32
+
+
+def assert_dgamma_parity(name, got, ref, abs_sum, chunk_rows: int, nchunks: int):
+    """|got - ref| <= 1e-4 |ref| (the bar), or within the fixed tree's forward-error
+    bound gamma * sum|terms| for columns whose sum cancels. Returns n_clause2."""
+    got = np.asarray(got, np.float64)
+    m1 = np.abs(got - ref) <= 1e-4 * np.abs(ref)
+    m2 = np.abs(got - ref) <= dgamma_bound_gamma(chunk_rows, nchunks) * abs_sum
+    ok = m1 | m2
+    if not ok.all():
+        i = int(np.argwhere(~ok)[0][0])
+        raise AssertionError(f"{name}: {np.count_nonzero(~ok)} columns outside tolerance; first {i}: "
+                             f"got {got[i]!r} ref {ref[i]!r} sum|t| {abs_sum[i]!r}")
+    return int(np.count_nonzero(m2 & ~m1))
