@@ -136,6 +136,29 @@ int rmsnorm_gated_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64
 int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D,
                           float* dgamma, rmsn_stream stream);
 
+/* Backward without a caller workspace (no counterpart in the pages: this is a
+ * library convenience). For callers that cannot allocate device memory — code
+ * that may only use the tensors it is handed, or a runtime that must not grow
+ * its device footprint after start-up — the weight-gradient scratch lives in a
+ * fixed array inside the library's device image: RMSN_NOALLOC_SCRATCH_BYTES on
+ * every GPU that loads the library, held until the process exits. The call
+ * allocates nothing; inputs and outputs are the caller's, as in rmsnorm_bwd
+ * (same arguments minus the workspace; dgamma must not be NULL).
+ *   - Problems needing more scratch than the array holds, i.e. with
+ *     rmsnorm_bwd_workspace_bytes(T, D) > RMSN_NOALLOC_SCRATCH_BYTES (for
+ *     example T > 32768 at D = 4096), are rejected with RMSN_EWORKSPACE.
+ *   - The first call on a device looks up the array's device address with
+ *     that device current; make that first call before any stream capture.
+ *   - Every call shares the one array: calls whose work overlaps on the GPU
+ *     (other streams or threads, unordered) race and corrupt dgamma. Calls on
+ *     one stream are safe. Leftover contents are never read.
+ *   - Results are bitwise those of rmsnorm_bwd on the same inputs. */
+#define RMSN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+int rmsnorm_bwd_noalloc(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                        const float* w, const float* rstd,
+                        rmsn_bf16* dx, int64_t lddx, float* dgamma,
+                        int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
 /* Reads the device-side error flags of the current device (OR of all kernels'
  * flags since the last clear) into *flags; clears them if `clear` is non-zero.
  * Synchronises with the device. 0 means no kernel ever gave up on a wait. */

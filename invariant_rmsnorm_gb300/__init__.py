@@ -29,13 +29,13 @@ __all__ = [
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
     "rmsnorm_gated_fwd", "rmsnorm_gated_bwd", "rmsnorm_dgamma_reduce",
     "rmsnorm_bwd_workspace_bytes", "rmsnorm_status_string", "rmsnorm_device_error",
-    "EXPORTED_SYMBOLS",
+    "rmsnorm_bwd_noalloc", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "rmsnorm_status_string", "rmsnorm_fwd", "rmsnorm_bwd_workspace_bytes", "rmsnorm_bwd",
     "rmsnorm_residual_fwd", "rmsnorm_residual_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
-    "rmsnorm_dgamma_reduce", "rmsnorm_device_error",
+    "rmsnorm_dgamma_reduce", "rmsnorm_device_error", "rmsnorm_bwd_noalloc",
 )
 
 _P = ctypes.c_void_p
@@ -57,6 +57,7 @@ _SIGS = {
                                  _SZ, _I64, _I64, _INT, _P]),
     "rmsnorm_dgamma_reduce": (_INT, [_P, _SZ, _I64, _I64, _P, _P]),
     "rmsnorm_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
+    "rmsnorm_bwd_noalloc": (_INT, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _I64, _INT, _P]),
 }
 
 _lock = threading.Lock()
@@ -227,6 +228,20 @@ def rmsnorm_dgamma_reduce(ws, T: int, D: int, dgamma, stream=None):
     wp, wb = _ws(ws)
     _check("rmsnorm_dgamma_reduce", load().rmsnorm_dgamma_reduce(
         wp, wb, int(T), int(D), _ptr(dgamma), _stream(stream, dgamma.device)))
+
+
+def rmsnorm_bwd_noalloc(g, x, w, rstd, dx, dgamma, zero_centered_gamma: bool = False, stream=None):
+    """Backward for callers that cannot allocate device memory: the library's own
+    fixed scratch array replaces the workspace (see include/rmsnorm.h)."""
+    T, D = x.shape
+    ldg, ldx, lddx = _act(g, "g", T, D), _act(x, "x", T, D), _act(dx, "dx", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    _check("rmsnorm_bwd_noalloc", load().rmsnorm_bwd_noalloc(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dgamma), T, D,
+        int(zero_centered_gamma), _stream(stream, x.device)))
 
 
 def rmsnorm_device_error(clear: bool = True) -> int:
