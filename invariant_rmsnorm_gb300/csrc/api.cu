@@ -16,14 +16,29 @@ namespace rmsn {
 // Row shape: a pure function of D (this is what makes a row's reduction tree,
 // and therefore its bits, independent of everything but D).
 // ---------------------------------------------------------------------------
+#ifndef RMSN_FWD_NTMAX
+#define RMSN_FWD_NTMAX 256
+#endif
+#ifndef RMSN_BWD_NTMAX
+#define RMSN_BWD_NTMAX 256
+#endif
+
+// Threads and 16-byte vectors per thread for one row of NV vectors: at most
+// `ntmax` threads (512 beyond 1024 vectors), VPT in {1, 2, 4}, threads rounded
+// up to whole warps; slots past the row end are idle.
+static void wide_shape(int NV, int ntmax, int* threads, int* vpt) {
+    if (NV > 4 * ntmax) ntmax = 512;
+    const int need = (NV + ntmax - 1) / ntmax;
+    *vpt = need <= 1 ? 1 : (need <= 2 ? 2 : 4);
+    *threads = ((NV + *vpt - 1) / *vpt + 31) / 32 * 32;
+}
+
 RowCfg row_cfg(int D) {
     RowCfg c{};
     const int NV = D / 8;  // 16-byte vectors per row
-    const int ntmax = NV > 1024 ? 512 : 256;
-    const int need = (NV + ntmax - 1) / ntmax;
     c.narrow = false;
-    c.vpt = need <= 1 ? 1 : (need <= 2 ? 2 : 4);
-    c.threads = ((NV + c.vpt - 1) / c.vpt + 31) / 32 * 32;
+    wide_shape(NV, RMSN_FWD_NTMAX, &c.threads, &c.vpt);
+    wide_shape(NV, RMSN_BWD_NTMAX, &c.bwd_threads, &c.bwd_vpt);
     c.group = 0;
     c.rows_per_stage = 1;
     c.chunk_rows = kWideChunkRows;

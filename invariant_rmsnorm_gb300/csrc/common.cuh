@@ -20,7 +20,10 @@ namespace rmsn {
 // Constants that fix the numerics. They depend on nothing but D, never on T,
 // the row index, the grid or the GPU's SM count.
 // ---------------------------------------------------------------------------
-constexpr int kWideChunkRows = 32;       // weight-gradient chunk (rows), wide path
+#ifndef RMSN_WIDE_CHUNK
+#define RMSN_WIDE_CHUNK 32
+#endif
+constexpr int kWideChunkRows = RMSN_WIDE_CHUNK;  // weight-gradient chunk (rows), wide path
 constexpr int kNarrowThreads = 256;      // narrow path CTA size
 constexpr int kNarrowChunkRowsMin = 64;  // weight-gradient chunk (rows), narrow path
 constexpr int kMaxD = 16384;
@@ -63,6 +66,24 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
 __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
     asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;"
                  ::"r"(smem_u32(bar)), "r"(bytes) : "memory");
+}
+
+// Plain arrive (release) on `bar`.
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Named barrier `id` over `nthreads` threads (a multiple of 32) that also
+// returns the AND of every participant's predicate.
+__device__ __forceinline__ int named_bar_and(int id, int nthreads, int pred) {
+    int res;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.s32 p, %1, 0;\n\t"
+        "bar.red.and.pred q, %2, %3, p;\n\t"
+        "selp.s32 %0, 1, 0, q;\n\t}"
+        : "=r"(res) : "r"(pred), "r"(id), "r"(nthreads) : "memory");
+    return res;
 }
 
 // Bounded wait for the phase with parity `parity` to complete. Returns false if
@@ -118,10 +139,14 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(map) : "memory");
 }
 
-// 4-byte asynchronous copy global -> shared whose completion is signalled on
-// `bar` by a no-increment arrive (the barrier's expected count includes it).
-__device__ __forceinline__ void cp_async4_arrive(void* dst, const void* src, uint64_t* bar) {
+// 4-byte asynchronous copy global -> shared (cp.async, L1-allocating).
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
     asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+
+// One arrive on `bar`, triggered once all of this thread's earlier cp.async
+// copies have landed; no-increment, so the barrier's expected count includes it.
+__device__ __forceinline__ void cp_async_arrive_noinc(uint64_t* bar) {
     asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
 

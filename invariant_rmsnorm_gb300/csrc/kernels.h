@@ -38,8 +38,10 @@ struct BwdArgs {
 // Row-shape configuration: a pure function of D.
 struct RowCfg {
     bool narrow;         // D <= 256: several rows per CTA, one lane group per row
-    int threads;         // CTA size
-    int vpt;             // 16-byte vectors per thread per row (wide); 1 (narrow)
+    int threads;         // CTA size (forward)
+    int vpt;             // 16-byte vectors per thread per row (wide forward); 1 (narrow)
+    int bwd_threads;     // CTA size (wide backward)
+    int bwd_vpt;         // 16-byte vectors per thread per row (wide backward)
     int group;           // lanes per row (narrow), a power of two <= 32
     int rows_per_stage;  // rows per pipeline stage (narrow); 1 (wide)
     int chunk_rows;      // rows per weight-gradient partial

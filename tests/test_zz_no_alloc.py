@@ -34,9 +34,25 @@ def _inputs(T, D, seed, zc):
     return g, x, w, rstd
 
 
+LIMIT = 16 << 20  # RMSN_NOALLOC_SCRATCH_BYTES
+
+
+def _largest_T(D):
+    """Largest T whose weight-gradient scratch still fits the library's array."""
+    lo, hi = 1, 1 << 24
+    while lo < hi:
+        mid = (lo + hi + 1) // 2
+        if rn.workspace_bytes(mid, D) <= LIMIT:
+            lo = mid
+        else:
+            hi = mid - 1
+    return lo
+
+
 def test_noalloc_backward_matches_workspace_backward():
-    cases = [(4096, 4096, 1, False), (32768, 4096, 2, False), (100, 2048, 3, True)]
-    assert rn.workspace_bytes(32768, 4096) == (16 << 20)  # the second call uses the whole array
+    t_full = _largest_T(4096)
+    assert rn.workspace_bytes(t_full, 4096) > LIMIT - 4 * 4096 * 64  # fills (almost) the whole array
+    cases = [(4096, 4096, 1, False), (t_full, 4096, 2, False), (100, 2048, 3, True)]
     for T, D, seed, zc in cases:
         g, x, w, rstd = _inputs(T, D, seed, zc)
         dx_ref = torch.empty_like(x)
@@ -52,7 +68,8 @@ def test_noalloc_backward_matches_workspace_backward():
 
 
 def test_noalloc_refuses_problems_larger_than_its_array():
-    T, D = 32769, 4096
+    D = 4096
+    T = _largest_T(D) + 1
     x = torch.zeros((T, D), dtype=torch.bfloat16, device=DEV)
     w = torch.ones(D, device=DEV)
     rstd = torch.ones(T, device=DEV)
