@@ -36,6 +36,18 @@ static void wide_shape(int NV, int ntmax, int* threads, int* vpt) {
 RowCfg row_cfg(int D) {
     RowCfg c{};
     const int NV = D / 8;  // 16-byte vectors per row
+    if (NV <= 32) {
+        // Narrow rows: one group of G lanes (a power of two) per row.
+        int G = 1;
+        while (G < NV) G *= 2;
+        c.narrow = true;
+        c.threads = c.bwd_threads = kNarrowThreads;
+        c.vpt = c.bwd_vpt = 1;
+        c.group = G;
+        c.rows_per_stage = narrow_stage_rows_for_group(G);
+        c.chunk_rows = narrow_chunk_rows_for_group(G);
+        return c;
+    }
     c.narrow = false;
     wide_shape(NV, RMSN_FWD_NTMAX, &c.threads, &c.vpt);
     wide_shape(NV, RMSN_BWD_NTMAX, &c.bwd_threads, &c.bwd_vpt);

@@ -25,7 +25,7 @@ namespace rmsn {
 #endif
 constexpr int kWideChunkRows = RMSN_WIDE_CHUNK;  // weight-gradient chunk (rows), wide path
 constexpr int kNarrowThreads = 256;      // narrow path CTA size
-constexpr int kNarrowChunkRowsMin = 64;  // weight-gradient chunk (rows), narrow path
+constexpr int kNarrowChunkRowsMin = 128;  // weight-gradient chunk (rows), narrow path (at least)
 constexpr int kMaxD = 16384;
 constexpr int kReduceWarps = 16;         // weight-gradient pass 2: warps per 32 columns
 

@@ -48,6 +48,8 @@ struct RowCfg {
 };
 
 RowCfg row_cfg(int D);
+int narrow_chunk_rows_for_group(int G);
+int narrow_stage_rows_for_group(int G);
 int64_t num_chunks(int64_t T, int D);
 
 // Launchers (return the launch's cudaError_t; arguments already validated).
