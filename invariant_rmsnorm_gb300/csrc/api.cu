@@ -161,13 +161,17 @@ int check_ws(const void* ws, size_t ws_bytes, int64_t T, int64_t D) {
 
 inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN_ECUDA; }
 
-int run_fwd(Mode m, const FwdArgs& a, cudaStream_t s) {
+float inv_pow2(int D) { return (D & (D - 1)) == 0 ? 1.0f / static_cast<float>(D) : 0.0f; }
+
+int run_fwd(Mode m, FwdArgs a, cudaStream_t s) {
+    a.inv_d_pow2 = inv_pow2(a.D);
     const RowCfg c = row_cfg(a.D);
     const cudaError_t e = c.narrow ? launch_narrow_fwd(m, a, c, s) : launch_wide_fwd(m, a, c, s);
     return cuda_status(e);
 }
 
-int run_bwd(Mode m, const BwdArgs& a, float* dgamma, cudaStream_t s) {
+int run_bwd(Mode m, BwdArgs a, float* dgamma, cudaStream_t s) {
+    a.inv_d_pow2 = inv_pow2(a.D);
     const RowCfg c = row_cfg(a.D);
     cudaError_t e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);
     if (e != cudaSuccess) return RMSN_ECUDA;

@@ -27,7 +27,7 @@ constexpr int kWideChunkRows = RMSN_WIDE_CHUNK;  // weight-gradient chunk (rows)
 constexpr int kNarrowThreads = 256;      // narrow path CTA size
 constexpr int kNarrowChunkRowsMin = 128;  // weight-gradient chunk (rows), narrow path (at least)
 constexpr int kMaxD = 16384;
-constexpr int kReduceWarps = 16;         // weight-gradient pass 2: warps per 32 columns
+constexpr int kReduceWarps = 32;         // weight-gradient pass 2: warps (chunk ranges) per 32 columns
 
 // Device-side error codes (bit flags OR-ed into the library's error words).
 constexpr unsigned kErrWaitTimeout = 1u;
@@ -157,6 +157,24 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// L2 policy for data written now and read back soon (kept resident in L2).
+__device__ __forceinline__ uint64_t policy_evict_last() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// 128-bit global store of four floats with an L2 cache policy.
+__device__ __forceinline__ void st_global_f4_hint(float* p, float a, float b, float c, float d, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.v4.f32 [%0], {%1, %2, %3, %4}, %5;"
+                 ::"l"(p), "f"(a), "f"(b), "f"(c), "f"(d), "l"(pol) : "memory");
+}
+
+// 32-bit global store with an L2 cache policy.
+__device__ __forceinline__ void st_global_f1_hint(float* p, float a, uint64_t pol) {
+    asm volatile("st.global.L2::cache_hint.f32 [%0], %1, %2;" ::"l"(p), "f"(a), "l"(pol) : "memory");
+}
+
 // 128-bit streaming global store.
 __device__ __forceinline__ void st_global_cs(void* p, uint4 v) {
     asm volatile("st.global.cs.v4.u32 [%0], {%1, %2, %3, %4};"
@@ -199,8 +217,16 @@ __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b)
 __device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
 __device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
 
-// sigmoid(z) = 1 / (1 + exp(-z)) in fp32 (CUDA expf, IEEE division).
-__device__ __forceinline__ float sigmoidf_rn(float z) { return __fdiv_rn(1.0f, fadd(1.0f, expf(-z))); }
+// sigmoid(z) = 1 / (1 + exp(-z)) in fp32: CUDA expf, then the correctly
+// rounded reciprocal (identical to the IEEE quotient 1/x, in fewer steps).
+__device__ __forceinline__ float sigmoidf_rn(float z) { return __frcp_rn(fadd(1.0f, expf(-z))); }
+
+// x / D, correctly rounded. When D is a power of two the host passes its exact
+// reciprocal `inv_pow2` and the quotient is that single exact scaling (same
+// bits as the division); otherwise inv_pow2 is 0 and an IEEE division runs.
+__device__ __forceinline__ float div_by_d(float x, int D, float inv_pow2) {
+    return inv_pow2 != 0.0f ? fmul(x, inv_pow2) : __fdiv_rn(x, static_cast<float>(D));
+}
 
 // Butterfly sum over aligned groups of WIDTH lanes (a power of two <= 32).
 // Every lane of a group ends with the same bits (IEEE addition commutes).

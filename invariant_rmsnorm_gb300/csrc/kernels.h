@@ -19,6 +19,7 @@ struct FwdArgs {
     float* rstd;
     uint16_t* xc; int64_t ldxc;         // input copy (residual)
     int64_t T; int D; float eps; int zc;
+    float inv_d_pow2;                   // 1/D if D is a power of two, else 0
 };
 
 // Everything a backward (pass 1) launch needs.
@@ -33,6 +34,7 @@ struct BwdArgs {
     uint16_t* dz; int64_t lddz;         // gated
     float* partials;                    // [nchunks][D] fp32 (workspace)
     int64_t T; int D; int zc;
+    float inv_d_pow2;                   // 1/D if D is a power of two, else 0
 };
 
 // Row-shape configuration: a pure function of D.

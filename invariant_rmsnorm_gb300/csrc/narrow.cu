@@ -249,7 +249,7 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fadd(ss, fmul(f[e], f[e]));
             ss = group_sum<G>(ss);
-            const float r = rsqrtf(fadd(__fdiv_rn(ss, static_cast<float>(D)), a.eps));
+            const float r = rsqrtf(fadd(div_by_d(ss, D, a.inv_d_pow2), a.eps));
             const int64_t row = row0 + rs_;
             if (row < T) {
                 if (l == 0) a.rstd[row] = r;
@@ -397,7 +397,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 sp = fadd(sp, fmul(gw[e], xf[e]));
             }
             sp = group_sum<G>(sp);
-            const float coef = fmul(__fdiv_rn(fmul(fmul(r, r), r), static_cast<float>(D)), sp);
+            const float coef = fmul(div_by_d(fmul(fmul(r, r), r), D, a.inv_d_pow2), sp);
             const int64_t row = row0 + rs_;
             if (row < T && lane_valid) {
                 float o[8];
@@ -439,10 +439,11 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 return;
             }
             const int64_t chunk = cta + static_cast<int64_t>(i / NSC) * Gd;
+            const uint64_t keep = policy_evict_last();  // re-read by pass 2 right away
             for (int col = tid; col < D; col += kNarrowThreads) {
                 float t = cb[col];
                 for (int q = 1; q < P; ++q) t = fadd(t, cb[q * D + col]);
-                a.partials[chunk * D + col] = t;
+                st_global_f1_hint(a.partials + chunk * D + col, t, keep);
             }
             cbuf ^= 1;
         }

@@ -298,7 +298,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
         for (int r = 0; r < R; ++r) {
             if (r < nvalid) {
                 const float tot = block_total<NWMAX>(rb + r * 32, nw);
-                const float rr = rsqrtf(fadd(__fdiv_rn(tot, static_cast<float>(D)), a.eps));
+                const float rr = rsqrtf(fadd(div_by_d(tot, D, a.inv_d_pow2), a.eps));
                 const int64_t row = cta + static_cast<int64_t>(i * R + r) * G;
                 if (tid == 0) a.rstd[row] = rr;
 #pragma unroll
@@ -495,7 +495,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             if (r < nvalid) {
                 const float r1 = rr[r];
                 const float s_tot = block_total<NWMAX>(rb + r * 32, nw);
-                const float coef = fmul(__fdiv_rn(fmul(fmul(r1, r1), r1), static_cast<float>(D)), s_tot);
+                const float coef = fmul(div_by_d(fmul(fmul(r1, r1), r1), D, a.inv_d_pow2), s_tot);
                 const int64_t row = row_of(i * R + r);
                 uint16_t* dxrow = a.dx + row * a.lddx;
 #pragma unroll
@@ -547,13 +547,15 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         const int k_last = i * R + nvalid - 1;
         if ((k_last % C) == C - 1 || k_last == n_my - 1) {
             const int64_t chunk = cta + static_cast<int64_t>(k_last / C) * G;
-            float4* prow = reinterpret_cast<float4*>(a.partials + chunk * D);
+            float* prow = a.partials + chunk * D;
+            // Partials are re-read by pass 2 right away: keep them in L2.
+            const uint64_t keep = policy_evict_last();
 #pragma unroll
             for (int j = 0; j < VPT; ++j) {
                 const int v = j * nt + tid;
                 if (v < NV) {
-                    prow[2 * v] = make_float4(acc[j][0], acc[j][1], acc[j][2], acc[j][3]);
-                    prow[2 * v + 1] = make_float4(acc[j][4], acc[j][5], acc[j][6], acc[j][7]);
+                    st_global_f4_hint(prow + 8 * v, acc[j][0], acc[j][1], acc[j][2], acc[j][3], keep);
+                    st_global_f4_hint(prow + 8 * v + 4, acc[j][4], acc[j][5], acc[j][6], acc[j][7], keep);
                 }
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;

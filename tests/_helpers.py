@@ -144,10 +144,10 @@ def assert_rel(name, got, ref, rtol):
                              f"got {got[i]!r} ref {ref[i]!r}")
 
 
-def dgamma_bound_gamma(chunk_rows: int, nchunks: int, reduce_warps: int = 16) -> float:
+def dgamma_bound_gamma(chunk_rows: int, nchunks: int, reduce_warps: int = 32) -> float:
     """Rounding-error factor of the library's fixed weight-gradient tree: products
-    (2-3 roundings, +8 for a gate), C sequential adds per chunk, ceil(n/16)
-    sequential adds per warp in pass 2, 16 warp totals."""
+    (2-3 roundings, +8 for a gate), C sequential adds per chunk, ceil(n/32)
+    sequential adds per warp in pass 2, 32 warp totals."""
     return (chunk_rows + -(-nchunks // reduce_warps) + reduce_warps + 8) * U32
 
 
