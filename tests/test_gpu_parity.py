@@ -219,3 +219,21 @@ def test_no_device_wait_ever_timed_out():
     import invariant_rmsnorm_gb300 as rn
     _full_check("residual", 256, 4096, seed=1)
     assert rn.rmsnorm_device_error(clear=True) == 0
+
+
+@pytest.mark.parametrize("D", [128, 2048])
+def test_gated_extreme_gates(D):
+    """Gates far out in both tails (|z| up to 100, where exp over- or underflows
+    in fp32) and exactly zero: the kernels' sigmoid stays finite and within the
+    tolerance of the oracle's double-precision one."""
+    T = 96
+    a = _inputs("gated", T, D, seed=21)
+    zf = torch.linspace(-100.0, 100.0, T * D, device=DEV).reshape(T, D)
+    zf[::7] = 0.0
+    z = zf[torch.randperm(T, generator=torch.Generator().manual_seed(3)).to(DEV)].to(torch.bfloat16)
+    fo = run_fwd("gated", a["x"], a["w"], 1e-6, True, z=z)
+    bo = run_bwd("gated", a["g"], a["x"], a["w"], fo["rstd"], True, z=z)
+    torch.cuda.synchronize()
+    assert torch.isfinite(fo["y"].float()).all() and torch.isfinite(bo["dz"].float()).all()
+    check_fwd("gated", a["x"], a["w"], 1e-6, True, fo, z=z, name="extreme gates")
+    check_bwd("gated", a["g"], a["x"], a["w"], fo["rstd"], True, bo, z=z, name="extreme gates")
