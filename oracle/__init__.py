@@ -40,7 +40,7 @@ from . import build as _build
 __all__ = [
     "round_bf16", "num_threads",
     "rmsnorm_fwd", "rmsnorm_bwd", "residual_fwd", "residual_bwd",
-    "gated_fwd", "gated_bwd", "weight_grad",
+    "gated_fwd", "gated_bwd", "weight_grad", "fused_add_fwd", "fused_add_bwd",
 ]
 
 _lock = threading.Lock()
@@ -65,8 +65,11 @@ def _load():
             lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
                                           _D, _D, _D, _D, _D]
             lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D, _D]
+            lib.orc_fused_add_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D, _D]
+            lib.orc_fused_add_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
+                                              _D, _D, _D]
             for f in ("orc_rmsnorm_fwd", "orc_rmsnorm_bwd", "orc_gated_fwd", "orc_gated_bwd",
-                      "orc_weight_grad"):
+                      "orc_weight_grad", "orc_fused_add_fwd", "orc_fused_add_bwd"):
                 getattr(lib, f).restype = None
             _lib = lib
     return _lib
@@ -209,3 +212,40 @@ def weight_grad(g, x, rstd, z=None, rounded: bool = True, with_abs: bool = False
     dwa = np.empty((D,)) if with_abs else None
     _load().orc_weight_grad(T, D, _p(g), _p(zz), _p(x), _p(rstd), int(rounded), _p(dw), _p(dwa))
     return (dw, dwa) if with_abs else dw
+
+
+def fused_add_fwd(x, res, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+    """Fused add + norm forward on h = x + res (fp32 sum). Returns ``(y, rstd, res_out)``
+    with ``res_out`` = bf16(h) (rounded mode) or h (unrounded)."""
+    x = _arr(x)
+    T, D = x.shape
+    res = _arr(res, (T, D))
+    w = _arr(w, (D,))
+    y = np.empty((T, D))
+    rstd = np.empty((T,))
+    ro = np.empty((T, D))
+    _load().orc_fused_add_fwd(T, D, _p(x), _p(res), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
+                              int(rounded), _p(y), _p(rstd), _p(ro))
+    return y, rstd, ro
+
+
+def fused_add_bwd(g, x, res, w, rstd, g_res=None, zero_centered_gamma: bool = False, rounded: bool = True,
+                  diagnostics: bool = False):
+    """Fused add + norm backward. Returns ``(dh [T,D], dgamma [D])`` (+ diagnostics as in
+    ``rmsnorm_bwd``); ``dh`` is the gradient of both x and res."""
+    x = _arr(x)
+    T, D = x.shape
+    g = _arr(g, (T, D))
+    res = _arr(res, (T, D))
+    w = _arr(w, (D,))
+    rstd = _arr(rstd, (T,))
+    gr = None if g_res is None else _arr(g_res, (T, D))
+    dh = np.empty((T, D))
+    dw = np.empty((D,))
+    hs = np.empty((T, D))
+    diag = {k: np.empty(s) for k, s in (("dx_pre", (T, D)), ("dx_scale", (T, D)), ("dw_abs", (D,)))} \
+        if diagnostics else {}
+    _load().orc_fused_add_bwd(T, D, _p(g), _p(x), _p(res), _p(w), _p(rstd), _p(gr), int(zero_centered_gamma),
+                              int(rounded), _p(dh), _p(dw), _p(hs), _p(diag.get("dx_pre")),
+                              _p(diag.get("dx_scale")), _p(diag.get("dw_abs")))
+    return (dh, dw, diag) if diagnostics else (dh, dw)

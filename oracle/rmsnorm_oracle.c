@@ -232,3 +232,45 @@ void orc_gated_bwd(int64_t T, int64_t D, const double* g, const double* x, const
     }
     orc_weight_grad(T, D, g, z, x, rstd, rounded, dw, dw_abs);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Fused add + RMSNorm (vLLM fused_add_rms_norm, the decoder-norm path of     */
+/* [ZC-norm], "Only layer 0's input norm takes the no-residual path"): the   */
+/* norm is applied to the fp32 sum h = x + res, which is also returned       */
+/* rounded to bf16 as the new residual stream.                               */
+/*   h = fl32(x + res);  res_out = bf16(h);  rstd, y as the plain forward on h */
+/* Reading (the pages give no rounding order): the sum is one fp32 add; the  */
+/* normalisation uses that fp32 h, not its bf16 rounding.                    */
+/* ------------------------------------------------------------------------ */
+void orc_fused_add_fwd(int64_t T, int64_t D, const double* x, const double* res, const double* w,
+                       double eps, int zero_centered, int rounded,
+                       double* y, double* rstd, double* res_out) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        double* h = res_out + t * D;  /* holds the unrounded sum until the end of the row */
+        for (int64_t j = 0; j < D; ++j) h[j] = maybe_fl32(x[t * D + j] + res[t * D + j], rounded);
+        double r = maybe_fl32(row_inv_rms(h, D, eps), rounded);
+        rstd[t] = r;
+        for (int64_t j = 0; j < D; ++j) {
+            y[t * D + j] = maybe_bf16(h[j] * r * w_eff(w[j], zero_centered, rounded), rounded);
+            h[j] = maybe_bf16(h[j], rounded);
+        }
+    }
+}
+
+/* Backward of the fused add + norm. The gradient reaching h is the plain     */
+/* backward at h plus the gradient of res_out (g_res, may be NULL = 0); it is */
+/* the gradient of both x and res (dh/dx = dh/dres = 1). The weight gradient  */
+/* is sum_t g_tj h_tj r_t. h is recomputed from x and res exactly as forward. */
+void orc_fused_add_bwd(int64_t T, int64_t D, const double* g, const double* x, const double* res,
+                       const double* w, const double* rstd, const double* g_res, int zero_centered,
+                       int rounded, double* dh, double* dw, double* h_scratch,
+                       double* dh_pre, double* dh_scale, double* dw_abs) {
+    /* h_scratch: caller-provided [T][D] buffer that receives h. */
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t)
+        for (int64_t j = 0; j < D; ++j)
+            h_scratch[t * D + j] = maybe_fl32(x[t * D + j] + res[t * D + j], rounded);
+    orc_rmsnorm_bwd(T, D, g, h_scratch, w, rstd, g_res, zero_centered, rounded, dh, dw, dh_pre, dh_scale,
+                    dw_abs);
+}

@@ -340,3 +340,47 @@ def test_weight_grad_column_subset_and_rows_order_free_of_layout():
     for j in range(D):
         exact = sum(Fraction(g[t, j]) * Fraction(x[t, j]) * Fraction(r[t]) for t in range(T))
         assert abs(Fraction(dw[j]) - exact) <= abs(exact) * Fraction(1, 2**23) + Fraction(1, 2**140)
+
+
+# ==========================================================================
+# Fused add + RMSNorm (the decoder-norm path of the zero-centred RMSNorm PR)
+# ==========================================================================
+
+def test_fused_add_bwd_matches_finite_differences():
+    """L = sum(g*y) + sum(g_res*res_out): the gradient of x and of res are the same
+    dh, and dgamma follows the plain form on h = x + res."""
+    x, w, g = _fd_setup(T=3, D=8)
+    res = RNG.standard_normal(x.shape)
+    gres = RNG.standard_normal(x.shape)
+
+    def loss():
+        y, _, ro = oracle.fused_add_fwd(x, res, w, 1e-6, rounded=False)
+        return float(np.sum(g * y) + np.sum(gres * ro))
+
+    _, r, _ = oracle.fused_add_fwd(x, res, w, 1e-6, rounded=False)
+    dh, dw = oracle.fused_add_bwd(g, x, res, w, r, g_res=gres, rounded=False)
+    assert np.abs(dh - fd_grad(loss, x)).max() < 2e-8
+    assert np.abs(dh - fd_grad(loss, res)).max() < 2e-8
+    assert np.abs(dw - fd_grad(loss, w)).max() < 2e-8
+
+
+@pytest.mark.parametrize("zc", [False, True])
+def test_fused_add_rounding_bruteforce(zc):
+    """res_out = RN_bf16(RN_fp32(x + res)) and y = RN_bf16(h32 * rstd * w_eff), with
+    rationals; the zero residual reduces to the plain forward bit for bit."""
+    T, D = 3, 16
+    x = _bf16_grid(RNG.standard_normal((T, D)))
+    res = _bf16_grid(RNG.standard_normal((T, D)) * 8)
+    w = np.float32(RNG.standard_normal(D) * 0.3).astype(np.float64)
+    y, rstd, ro = oracle.fused_add_fwd(x, res, w, 1e-6, zero_centered_gamma=zc)
+    weff = (np.float32(w) + np.float32(1.0)).astype(np.float64) if zc else w
+    for t in range(T):
+        for j in range(D):
+            h32 = float(np.float32(Fraction(x[t, j]) + Fraction(res[t, j])))  # x + res is exact in double
+            assert ro[t, j] == bf16_round_bruteforce(Fraction(h32))
+            assert y[t, j] == bf16_round_bruteforce(Fraction(h32) * Fraction(rstd[t]) * Fraction(weff[j]))
+    y0, r0, ro0 = oracle.fused_add_fwd(x, np.zeros_like(x), w, 1e-6, zero_centered_gamma=zc)
+    yp, rp = oracle.rmsnorm_fwd(x, w, 1e-6, zero_centered_gamma=zc)
+    np.testing.assert_array_equal(y0, yp)
+    np.testing.assert_array_equal(r0, rp)
+    np.testing.assert_array_equal(ro0, x)
