@@ -402,6 +402,23 @@ def side_measurements(rn, synth, dev, stream, reps=50):
         rn.rmsnorm_gated_fwd(g.x, g.z, g.w, y, r, EPS, True, stream=stream)
         rn.rmsnorm_gated_bwd(g.g, g.x, g.z, g.w, r, dx, dz, dw, ws, True, stream=stream)
     res["gated_262144x128_fwd_bwd_gbs"] = _time_gbs(gated, T * (16 * D + 8), reps, stream)
+    del g, y, dx, dz
+    # fused add + norm at the decoder shape, 32768 x 2048: 18*D + 8 bytes per row
+    # (x, res in; y, res_out, rstd out; g, x, res, g_res, rstd in; dh out)
+    T, D = 32768, 2048
+    x = synth.normal_bf16((T, D), 5, dev)
+    rs = synth.normal_bf16((T, D), 6, dev, std=4.0)
+    gg = synth.normal_bf16((T, D), 7, dev)
+    gr = synth.normal_bf16((T, D), 8, dev)
+    w = synth.gamma_f32(D, 9, dev)
+    y, ro, dh = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    r, dw = torch.empty(T, device=dev), torch.empty(D, device=dev)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+
+    def fused():
+        rn.rmsnorm_fused_add_fwd(x, rs, w, y, r, ro, EPS, False, stream=stream)
+        rn.rmsnorm_fused_add_bwd(gg, x, rs, w, r, gr, dh, dw, ws, False, stream=stream)
+    res["fused_add_32768x2048_fwd_bwd_gbs"] = _time_gbs(fused, T * (18 * D + 8), reps, stream)
     return res
 
 

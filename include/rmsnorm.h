@@ -130,6 +130,30 @@ int rmsnorm_gated_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64
                       void* ws, size_t ws_bytes,
                       int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
 
+/* Fused add + RMSNorm, the decoder-norm path of Qwen3-Next ([ZC-norm]: all
+ * decoder norms but layer 0's input norm add the residual stream first and
+ * normalise the fp32 sum). Forward, per element and row:
+ *   h = x + res (one fp32 add);  res_out = bf16(h)  (the new residual stream);
+ *   rstd, y as rmsnorm_fwd applied to the fp32 h (not to its bf16 rounding).
+ *   x, res [T][ld*] in; y, res_out [T][ld*] out; rstd [T] out. */
+int rmsnorm_fused_add_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* res, int64_t ldres,
+                          const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
+                          rmsn_bf16* res_out, int64_t ldro,
+                          int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                          rmsn_stream stream);
+
+/* Fused add + RMSNorm backward. h is recomputed from x and res exactly as in
+ * the forward; with g = dL/dy and g_res = dL/d res_out (NULL = zero), the
+ * gradient of h (and so of both x and res) is
+ *   dh = bf16( rmsnorm backward at h  +  g_res ),   dgamma_j = sum_t g_tj h_tj r_t.
+ * Workspace and dgamma == NULL as in rmsnorm_bwd. */
+int rmsnorm_fused_add_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                          const rmsn_bf16* res, int64_t ldres, const float* w, const float* rstd,
+                          const rmsn_bf16* g_res, int64_t ldgr,
+                          rmsn_bf16* dh, int64_t lddh, float* dgamma,
+                          void* ws, size_t ws_bytes,
+                          int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
 /* Weight-gradient pass 2 on its own: sums the per-chunk partials that a backward
  * call with a NULL dgamma/dw left in ws (same T, D and workspace), in the fixed
  * order, into dgamma [D]. ws must be unchanged since that call. */

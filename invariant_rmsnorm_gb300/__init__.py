@@ -29,13 +29,14 @@ __all__ = [
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
     "rmsnorm_gated_fwd", "rmsnorm_gated_bwd", "rmsnorm_dgamma_reduce",
     "rmsnorm_bwd_workspace_bytes", "rmsnorm_status_string", "rmsnorm_device_error",
-    "rmsnorm_bwd_noalloc", "EXPORTED_SYMBOLS",
+    "rmsnorm_bwd_noalloc", "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "rmsnorm_status_string", "rmsnorm_fwd", "rmsnorm_bwd_workspace_bytes", "rmsnorm_bwd",
     "rmsnorm_residual_fwd", "rmsnorm_residual_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
     "rmsnorm_dgamma_reduce", "rmsnorm_device_error", "rmsnorm_bwd_noalloc",
+    "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd",
 )
 
 _P = ctypes.c_void_p
@@ -58,6 +59,9 @@ _SIGS = {
     "rmsnorm_dgamma_reduce": (_INT, [_P, _SZ, _I64, _I64, _P, _P]),
     "rmsnorm_device_error": (_INT, [ctypes.POINTER(ctypes.c_uint), _INT]),
     "rmsnorm_bwd_noalloc": (_INT, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _I64, _INT, _P]),
+    "rmsnorm_fused_add_fwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _F, _INT, _P]),
+    "rmsnorm_fused_add_bwd": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _SZ,
+                                     _I64, _I64, _INT, _P]),
 }
 
 _lock = threading.Lock()
@@ -221,6 +225,34 @@ def rmsnorm_gated_bwd(g, x, z, w, rstd, dx, dz, dw, ws, zero_centered_gamma: boo
     _check("rmsnorm_gated_bwd", load().rmsnorm_gated_bwd(
         _ptr(g), ldg, _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dz), lddz,
         _ptr(dw), wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_fused_add_fwd(x, res, w, y, rstd, res_out, eps: float = 1e-6, zero_centered_gamma: bool = False,
+                          stream=None):
+    """Norm of h = x + res (fp32); also writes bf16(h) to ``res_out``."""
+    T, D = x.shape
+    ldx, ldr, ldy, ldo = _act(x, "x", T, D), _act(res, "res", T, D), _act(y, "y", T, D), _act(res_out, "res_out", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_fused_add_fwd", load().rmsnorm_fused_add_fwd(
+        _ptr(x), ldx, _ptr(res), ldr, _ptr(w), _ptr(y), ldy, _ptr(rstd), _ptr(res_out), ldo, T, D, float(eps),
+        int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_fused_add_bwd(g, x, res, w, rstd, g_res, dh, dgamma, ws, zero_centered_gamma: bool = False,
+                          stream=None):
+    """Gradient of h = x + res (that of both x and res); ``g_res`` may be None."""
+    T, D = x.shape
+    ldg, ldx, ldr, ldd = _act(g, "g", T, D), _act(x, "x", T, D), _act(res, "res", T, D), _act(dh, "dh", T, D)
+    ldgr = _act(g_res, "g_res", T, D) if g_res is not None else D
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_fused_add_bwd", load().rmsnorm_fused_add_bwd(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(res), ldr, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dh), ldd,
+        _ptr(dgamma), wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
 
 
 def rmsnorm_dgamma_reduce(ws, T: int, D: int, dgamma, stream=None):

@@ -314,6 +314,47 @@ int rmsnorm_gated_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64
     return run_bwd(kGated, a, dw, stream);
 }
 
+int rmsnorm_fused_add_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* res, int64_t ldres, const float* w,
+                          rmsn_bf16* y, int64_t ldy, float* rstd, rmsn_bf16* res_out, int64_t ldro, int64_t T,
+                          int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(res, ldres, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_act(res_out, ldro, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.res = res; a.ldres = ldres; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.xc = res_out; a.ldxc = ldro;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kFusedAdd, a, stream);
+}
+
+int rmsnorm_fused_add_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* res,
+                          int64_t ldres, const float* w, const float* rstd, const rmsn_bf16* g_res, int64_t ldgr,
+                          rmsn_bf16* dh, int64_t lddh, float* dgamma, void* ws, size_t ws_bytes, int64_t T,
+                          int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(res, ldres, D));
+    RMSN_TRY(check_act(dh, lddh, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.res = res; a.ldres = ldres; a.gres = g_res; a.ldgr = ldgr;
+    a.w = w; a.rstd = rstd; a.dx = dh; a.lddx = lddh; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(g_res ? kFusedAdd : kFusedAddNoGres, a, dgamma, stream);
+}
+
 int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D, float* dgamma,
                           rmsn_stream stream) {
     RMSN_TRY(check_shape(T, D));

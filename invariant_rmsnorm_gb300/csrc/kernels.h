@@ -8,7 +8,17 @@
 
 namespace rmsn {
 
-enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2 };
+// kFusedAdd / kFusedAddNoGres: the norm of h = x + res (fp32), forward also
+// returning bf16(h); the backward with or without the gradient of that output.
+enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2, kFusedAdd = 3, kFusedAddNoGres = 4 };
+
+// Operands streamed per row, by mode.
+__host__ __device__ constexpr int fwd_inputs(int mode) { return (mode == kGated || mode >= kFusedAdd) ? 2 : 1; }
+__host__ __device__ constexpr int bwd_inputs(int mode) {
+    return mode == kPlain ? 2 : (mode == kResidual || mode == kGated || mode == kFusedAddNoGres) ? 3 : 4;
+}
+__host__ __device__ constexpr bool is_fused(int mode) { return mode >= kFusedAdd; }
+__host__ __device__ constexpr bool has_gres(int mode) { return mode == kResidual || mode == kFusedAdd; }
 
 // Everything a forward launch needs (unused pointers are null).
 struct FwdArgs {
@@ -17,7 +27,8 @@ struct FwdArgs {
     const float* w;
     uint16_t* y; int64_t ldy;
     float* rstd;
-    uint16_t* xc; int64_t ldxc;         // input copy (residual)
+    uint16_t* xc; int64_t ldxc;         // input copy (residual) / bf16(x + res) (fused add)
+    const uint16_t* res; int64_t ldres; // residual stream (fused add)
     int64_t T; int D; float eps; int zc;
     float inv_d_pow2;                   // 1/D if D is a power of two, else 0
 };
@@ -27,7 +38,8 @@ struct BwdArgs {
     const uint16_t* g; int64_t ldg;
     const uint16_t* x; int64_t ldx;
     const uint16_t* z; int64_t ldz;     // gate (gated)
-    const uint16_t* gres; int64_t ldgr; // gradient of the input copy (residual)
+    const uint16_t* gres; int64_t ldgr; // gradient of the input copy (residual) / of bf16(x+res) (fused)
+    const uint16_t* res; int64_t ldres; // residual stream (fused add)
     const float* w;
     const float* rstd;
     uint16_t* dx; int64_t lddx;

@@ -110,17 +110,32 @@ namespace {
 // The operands' tensor maps, passed by value as one grid-constant parameter.
 struct NarrowMaps {
     CUtensorMap a;     // x (forward) / g (backward)
-    CUtensorMap b;     // z (gated forward) / x (backward)
-    CUtensorMap c;     // g_res or z (backward)
+    CUtensorMap b;     // z or res (forward) / x (backward)
+    CUtensorMap c;     // g_res, z or res (backward)
+    CUtensorMap d;     // g_res (fused-add backward)
     CUtensorMap rstd;  // backward
 };
+
+// The values a row is normalised over: x, or the fp32 sum x + res (fused add).
+template <int MODE>
+__device__ __forceinline__ void narrow_norm_input(const uint4 xv, const uint4 sv, float (&f)[8]) {
+    unpack8(xv, f);
+    if (is_fused(MODE)) {
+        float rv[8];
+        unpack8(sv, rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = fadd(f[e], rv[e]);
+    }
+}
 
 constexpr int kNarrowConsumerBarrier = 1;
 
 // Rows of one pass (P), of one stage (RS) and of one weight-gradient chunk (CN).
 template <int G> __host__ __device__ constexpr int narrow_pass_rows() { return kNarrowThreads / G; }
+// Rows of 256 B < 2D <= 512 B use 32-row stages so that two stages of four
+// operands still fit in shared memory; narrower rows use 64 (or P).
 template <int G> __host__ __device__ constexpr int narrow_stage_rows() {
-    return narrow_pass_rows<G>() > 64 ? narrow_pass_rows<G>() : 64;
+    return G == 32 ? 32 : (narrow_pass_rows<G>() > 64 ? narrow_pass_rows<G>() : 64);
 }
 template <int G> __host__ __device__ constexpr int narrow_chunk_rows() {
     return narrow_stage_rows<G>() > kNarrowChunkRowsMin ? narrow_stage_rows<G>() : kNarrowChunkRowsMin;
@@ -172,7 +187,7 @@ __device__ __forceinline__ void load_weights8(const float* w, int zc, bool valid
 template <int MODE, int G>
 __global__ void __launch_bounds__(kNarrowThreads + 32)
 narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const int S) {
-    constexpr int NIN = (MODE == kGated) ? 2 : 1;
+    constexpr int NIN = fwd_inputs(MODE);
     constexpr int P = narrow_pass_rows<G>();
     constexpr int RS = narrow_stage_rows<G>();
     constexpr int NP = RS / P;
@@ -205,14 +220,14 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
     if (warp == kNarrowThreads / 32) {  // producer warp
         if (lane == 0) {
             prefetch_tensormap(&m.a);
-            if (MODE == kGated) prefetch_tensormap(&m.b);
+            if (NIN == 2) prefetch_tensormap(&m.b);
             const uint64_t pol = policy_evict_first();
             narrow_produce(full, empty, S, n_it, [&](int i, int s) {
                 unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
                 const int row0 = (cta + i * Gd) * RS;
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tensor2d_g2s(st, &m.a, 0, row0, &full[s], pol);
-                if (MODE == kGated) tensor2d_g2s(st + tile_bytes, &m.b, 0, row0, &full[s], pol);
+                if (NIN == 2) tensor2d_g2s(st + tile_bytes, &m.b, 0, row0, &full[s], pol);
             });
         }
         return;
@@ -237,14 +252,14 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
             uint4 xv = make_uint4(0, 0, 0, 0), zv = make_uint4(0, 0, 0, 0);
             if (lane_valid) {
                 xv = ld_shared_v4(st + (static_cast<size_t>(rs_) * D + 8 * l) * 2);
-                if (MODE == kGated) zv = ld_shared_v4(st + tile_bytes + (static_cast<size_t>(rs_) * D + 8 * l) * 2);
+                if (NIN == 2) zv = ld_shared_v4(st + tile_bytes + (static_cast<size_t>(rs_) * D + 8 * l) * 2);
             }
             if (p == NP - 1) {  // whole stage read: release it
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
             float f[8];
-            unpack8(xv, f);
+            narrow_norm_input<MODE>(xv, zv, f);  // x, or h = x + res
             float ss = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fadd(ss, fmul(f[e], f[e]));
@@ -269,6 +284,7 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
                     }
                     st_global_cs(a.y + row * a.ldy + 8 * l, pack8(o));
                     if (MODE == kResidual) st_global_cs(a.xc + row * a.ldxc + 8 * l, xv);
+                    if (is_fused(MODE)) st_global_cs(a.xc + row * a.ldxc + 8 * l, pack8(f));  // bf16(x + res)
                 }
             }
         }
@@ -285,7 +301,7 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
 template <int MODE, int G>
 __global__ void __launch_bounds__(kNarrowThreads + 32)
 narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const int S) {
-    constexpr int NIN = (MODE == kPlain) ? 2 : 3;
+    constexpr int NIN = bwd_inputs(MODE);
     constexpr int P = narrow_pass_rows<G>();
     constexpr int RS = narrow_stage_rows<G>();
     constexpr int NP = RS / P;
@@ -332,7 +348,8 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
         if (lane == 0) {
             prefetch_tensormap(&m.a);
             prefetch_tensormap(&m.b);
-            if (MODE != kPlain) prefetch_tensormap(&m.c);
+            if (NIN >= 3) prefetch_tensormap(&m.c);
+            if (NIN == 4) prefetch_tensormap(&m.d);
             prefetch_tensormap(&m.rstd);
             const uint64_t pol = policy_evict_first();
             narrow_produce(full, empty, S, n_it, [&](int i, int s) {
@@ -341,7 +358,8 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 mbar_arrive_expect_tx(&full[s], stage_bytes);
                 tensor2d_g2s(st, &m.a, 0, row0, &full[s], pol);
                 tensor2d_g2s(st + tile_bytes, &m.b, 0, row0, &full[s], pol);
-                if (MODE != kPlain) tensor2d_g2s(st + 2 * tile_bytes, &m.c, 0, row0, &full[s], pol);
+                if (NIN >= 3) tensor2d_g2s(st + 2 * tile_bytes, &m.c, 0, row0, &full[s], pol);
+                if (NIN == 4) tensor2d_g2s(st + 3 * tile_bytes, &m.d, 0, row0, &full[s], pol);
                 tensor1d_g2s(st + NIN * tile_bytes, &m.rstd, row0, &full[s], pol);
             });
         }
@@ -365,22 +383,24 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
 #pragma unroll
         for (int p = 0; p < NP; ++p) {
             const int rs_ = p * P + gr;
-            uint4 gv = make_uint4(0, 0, 0, 0), xv = gv, tv = gv;
+            uint4 gv = make_uint4(0, 0, 0, 0), xv = gv, tv = gv, fv = gv;
             if (lane_valid) {
                 const size_t off = (static_cast<size_t>(rs_) * D + 8 * l) * 2;
                 gv = ld_shared_v4(st + off);
                 xv = ld_shared_v4(st + tile_bytes + off);
-                if (MODE != kPlain) tv = ld_shared_v4(st + 2 * tile_bytes + off);
+                if (NIN >= 3) tv = ld_shared_v4(st + 2 * tile_bytes + off);
+                if (NIN == 4) fv = ld_shared_v4(st + 3 * tile_bytes + off);
             }
             const float r = rtile[rs_];
             if (p == NP - 1) {  // whole stage read: release it
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
-            float gf[8], xf[8], tf[8], sg[8], g0[8];
+            float gf[8], xf[8], tf[8], sg[8], g0[8], ff[8];
             unpack8(gv, gf);
-            unpack8(xv, xf);
-            if (MODE != kPlain) unpack8(tv, tf);
+            narrow_norm_input<MODE>(xv, tv, xf);  // x, or h = x + res
+            if (MODE == kResidual || MODE == kGated) unpack8(tv, tf);
+            if (MODE == kFusedAdd) unpack8(fv, ff);
             if (MODE == kGated) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) {
@@ -405,6 +425,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 for (int e = 0; e < 8; ++e) {
                     float d = fsub(fmul(gw[e], r), fmul(xf[e], coef));
                     if (MODE == kResidual) d = fadd(d, tf[e]);
+                    if (MODE == kFusedAdd) d = fadd(d, ff[e]);
                     o[e] = d;
                     acc[e] = fadd(acc[e], fmul(fmul(gf[e], xf[e]), r));
                 }
@@ -467,11 +488,12 @@ int narrow_stages(size_t budget, size_t stage, size_t fixed) {
 template <int MODE, int G>
 cudaError_t nfwd_t(const FwdArgs& a, cudaStream_t st) {
     constexpr int RS = narrow_stage_rows<G>();
-    constexpr int NIN = (MODE == kGated) ? 2 : 1;
+    constexpr int NIN = fwd_inputs(MODE);
     NarrowMaps m;
     std::memset(&m, 0, sizeof(m));
     cudaError_t e = encode_rows_2d(&m.a, a.x, a.T, a.D, a.ldx, RS);
     if (e == cudaSuccess && MODE == kGated) e = encode_rows_2d(&m.b, a.z, a.T, a.D, a.ldz, RS);
+    if (e == cudaSuccess && is_fused(MODE)) e = encode_rows_2d(&m.b, a.res, a.T, a.D, a.ldres, RS);
     if (e != cudaSuccess) return e;
     const size_t stage = static_cast<size_t>(NIN) * RS * a.D * 2;
     const int S = narrow_stages(RMSN_NARROW_FWD_SMEM, stage, 0);
@@ -494,13 +516,15 @@ cudaError_t nbwd_t(const BwdArgs& a, cudaStream_t st) {
     constexpr int RS = narrow_stage_rows<G>();
     constexpr int CN = narrow_chunk_rows<G>();
     constexpr int P = narrow_pass_rows<G>();
-    constexpr int NIN = (MODE == kPlain) ? 2 : 3;
+    constexpr int NIN = bwd_inputs(MODE);
     NarrowMaps m;
     std::memset(&m, 0, sizeof(m));
     cudaError_t e = encode_rows_2d(&m.a, a.g, a.T, a.D, a.ldg, RS);
     if (e == cudaSuccess) e = encode_rows_2d(&m.b, a.x, a.T, a.D, a.ldx, RS);
     if (e == cudaSuccess && MODE == kResidual) e = encode_rows_2d(&m.c, a.gres, a.T, a.D, a.ldgr, RS);
     if (e == cudaSuccess && MODE == kGated) e = encode_rows_2d(&m.c, a.z, a.T, a.D, a.ldz, RS);
+    if (e == cudaSuccess && is_fused(MODE)) e = encode_rows_2d(&m.c, a.res, a.T, a.D, a.ldres, RS);
+    if (e == cudaSuccess && MODE == kFusedAdd) e = encode_rows_2d(&m.d, a.gres, a.T, a.D, a.ldgr, RS);
     if (e == cudaSuccess) e = encode_vec_1d(&m.rstd, a.rstd, a.T, RS);
     if (e != cudaSuccess) return e;
     const size_t stage = static_cast<size_t>(NIN) * RS * a.D * 2 + RS * 4;
@@ -575,6 +599,8 @@ cudaError_t launch_narrow_fwd(Mode md, const FwdArgs& a, const RowCfg& c, cudaSt
         case kPlain: return nfwd_dispatch<kPlain>(a, c, st);
         case kResidual: return nfwd_dispatch<kResidual>(a, c, st);
         case kGated: return nfwd_dispatch<kGated>(a, c, st);
+        case kFusedAdd:
+        case kFusedAddNoGres: return nfwd_dispatch<kFusedAdd>(a, c, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -584,6 +610,8 @@ cudaError_t launch_narrow_bwd(Mode md, const BwdArgs& a, const RowCfg& c, cudaSt
         case kPlain: return nbwd_dispatch<kPlain>(a, c, st);
         case kResidual: return nbwd_dispatch<kResidual>(a, c, st);
         case kGated: return nbwd_dispatch<kGated>(a, c, st);
+        case kFusedAdd: return nbwd_dispatch<kFusedAdd>(a, c, st);
+        case kFusedAddNoGres: return nbwd_dispatch<kFusedAddNoGres>(a, c, st);
     }
     return cudaErrorInvalidValue;
 }

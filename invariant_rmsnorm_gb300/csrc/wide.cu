@@ -121,6 +121,18 @@ __device__ __forceinline__ void load_weights(const float* w, int zc, int NV, int
     }
 }
 
+// The values a row is normalised over: x, or the fp32 sum x + res (fused add).
+template <int MODE>
+__device__ __forceinline__ void norm_input(const uint4 xv, const uint4 sv, float (&f)[8]) {
+    unpack8(xv, f);
+    if (is_fused(MODE)) {
+        float rv[8];
+        unpack8(sv, rv);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) f[e] = fadd(f[e], rv[e]);
+    }
+}
+
 // First half of the block-wide fixed tree, for R rows at once: butterfly
 // within each consumer warp (the R chains interleave), lane 0 parks each warp
 // total in red[r*32 + warp]. The consumers' named barrier doubles as the error
@@ -191,7 +203,7 @@ __device__ void consumer_abort(uint64_t* full, int S, int i, int n_it) {
 // ---------------------------------------------------------------------------
 template <int VPT, int MODE, int MAXT>
 __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, const int S) {
-    constexpr int NIN = (MODE == kGated) ? 2 : 1;
+    constexpr int NIN = fwd_inputs(MODE);
     constexpr int R = fwd_rows<VPT>();
     constexpr int NWMAX = MAXT / 32;
     extern __shared__ __align__(128) unsigned char smem[];
@@ -233,6 +245,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                     unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
                     bulk_g2s(dst, a.x + row * a.ldx, row_bytes, &full[s], pol);
                     if (MODE == kGated) bulk_g2s(dst + row_bytes, a.z + row * a.ldz, row_bytes, &full[s], pol);
+                    if (is_fused(MODE)) bulk_g2s(dst + row_bytes, a.res + row * a.ldres, row_bytes, &full[s], pol);
                 }
             });
         }
@@ -250,7 +263,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
         const int nvalid = min(n_my - i * R, R);
 
         uint4 xv[R][VPT];
-        uint4 zv[R][VPT];
+        uint4 zv[R][VPT];  // gated: z; fused add: res
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             if (r < nvalid) {
@@ -260,7 +273,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                     const int v = j * nt + tid;
                     if (v < NV) {
                         xv[r][j] = ld_shared_v4(src + 16 * v);
-                        if (MODE == kGated) zv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
+                        if (NIN == 2) zv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
                     }
                 }
             }
@@ -282,7 +295,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                 for (int j = 0; j < VPT; ++j) {
                     if (j * nt + tid < NV) {
                         float f[8];
-                        unpack8(xv[r][j], f);
+                        norm_input<MODE>(xv[r][j], zv[r][j], f);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) ss[r] = fadd(ss[r], fmul(f[e], f[e]));
                     }
@@ -306,7 +319,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                     const int v = j * nt + tid;
                     if (v < NV) {
                         float f[8], o[8];
-                        unpack8(xv[r][j], f);
+                        norm_input<MODE>(xv[r][j], zv[r][j], f);
                         if (MODE == kGated) {
                             float zf[8];
                             unpack8(zv[r][j], zf);
@@ -321,6 +334,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                         }
                         st_global_cs(a.y + row * a.ldy + 8 * v, pack8(o));
                         if (MODE == kResidual) st_global_cs(a.xc + row * a.ldxc + 8 * v, xv[r][j]);
+                        if (is_fused(MODE)) st_global_cs(a.xc + row * a.ldxc + 8 * v, pack8(f));  // bf16(x + res)
                     }
                 }
             }
@@ -341,7 +355,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
 template <int VPT, int MODE, int MAXT>
 __global__ void __launch_bounds__(MAXT + 32, ((MAXT <= 256 && VPT <= 2) ? RMSN_BWD_MINB : 1))
 wide_bwd_kernel(const BwdArgs a, const int S) {
-    constexpr int NIN = (MODE == kPlain) ? 2 : 3;
+    constexpr int NIN = bwd_inputs(MODE);
     constexpr int C = kWideChunkRows;
     constexpr int R = bwd_rows<VPT, MAXT>();
     constexpr int NWMAX = MAXT / 32;
@@ -388,8 +402,9 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     if (warp == nw) {  // producer warp
         if (lane == 0) {
             const uint64_t pol = policy_evict_first();
-            const uint16_t* third = (MODE == kResidual) ? a.gres : a.z;
-            const int64_t ld_third = (MODE == kResidual) ? a.ldgr : a.ldz;
+            // Operands after g and x: residual g_res; gated z; fused add res, then g_res.
+            const uint16_t* third = (MODE == kResidual) ? a.gres : (MODE == kGated ? a.z : a.res);
+            const int64_t ld_third = (MODE == kResidual) ? a.ldgr : (MODE == kGated ? a.ldz : a.ldres);
             produce(full, empty, S, n_it, [&](int i, int s) {
                 unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
                 const int nvalid = min(n_my - i * R, R);
@@ -401,8 +416,9 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                     unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
                     bulk_g2s(dst, a.g + row * a.ldg, row_bytes, &full[s], pol);
                     bulk_g2s(dst + row_bytes, a.x + row * a.ldx, row_bytes, &full[s], pol);
-                    if (MODE != kPlain)
+                    if (NIN >= 3)
                         bulk_g2s(dst + 2 * row_bytes, third + row * ld_third, row_bytes, &full[s], pol);
+                    if (NIN == 4) bulk_g2s(dst + 3 * row_bytes, a.gres + row * a.ldgr, row_bytes, &full[s], pol);
                 }
             });
         }
@@ -427,11 +443,11 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         float gw[R][VPT][8];  // g*w_eff   (gated: g*silu(z)*w_eff)
         float xs[R][VPT][8];  // x
         float gx[R][VPT][8];  // g*x       (gated: g*silu(z)*x)
-        float tz[R][VPT][8];  // residual: g_res; gated: z
+        float tz[R][VPT][8];  // residual: g_res; gated: z; fused add: res
         float g0[R][VPT][8];  // gated: g
         float rr[R];
         float sp[R];          // this thread's part of s = sum g x w_eff (gated: g q x w_eff)
-        uint4 gv[R][VPT], xv[R][VPT], tv[R][VPT];
+        uint4 gv[R][VPT], xv[R][VPT], tv[R][VPT], fv[R][VPT];  // fv: fused add's g_res
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             rr[r] = 0.0f;
@@ -444,7 +460,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                     if (v < NV) {
                         gv[r][j] = ld_shared_v4(src + 16 * v);
                         xv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
-                        if (MODE != kPlain) tv[r][j] = ld_shared_v4(src + 2 * row_bytes + 16 * v);
+                        if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_bytes + 16 * v);
+                        if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
                     }
                 }
             }
@@ -466,8 +483,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                     if (j * nt + tid < NV) {
                         float gf[8];
                         unpack8(gv[r][j], gf);
-                        unpack8(xv[r][j], xs[r][j]);
-                        if (MODE != kPlain) unpack8(tv[r][j], tz[r][j]);
+                        norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);  // x, or h = x + res
+                        if (MODE == kResidual || MODE == kGated) unpack8(tv[r][j], tz[r][j]);
                         if (MODE == kGated) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
@@ -506,8 +523,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             // Recompute the phase-1 products from the packed row (same bits).
                             float gf[8];
                             unpack8(gv[r][j], gf);
-                            unpack8(xv[r][j], xs[r][j]);
-                            if (MODE != kPlain) unpack8(tv[r][j], tz[r][j]);
+                            norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
+                            if (MODE == kResidual || MODE == kGated) unpack8(tv[r][j], tz[r][j]);
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 if (MODE == kGated) {
@@ -518,11 +535,13 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                 gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
                             }
                         }
-                        float o[8];
+                        float o[8], fg[8];
+                        if (MODE == kFusedAdd) unpack8(fv[r][j], fg);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             float d = fsub(fmul(gw[r][j][e], r1), fmul(xs[r][j][e], coef));
                             if (MODE == kResidual) d = fadd(d, tz[r][j][e]);
+                            if (MODE == kFusedAdd) d = fadd(d, fg[e]);
                             o[e] = d;
                             acc[j][e] = fadd(acc[j][e], fmul(gx[r][j][e], r1));
                         }
@@ -581,7 +600,7 @@ inline int stages_for(size_t budget, size_t stage_bytes, size_t per_stage_extra,
 
 template <int VPT, int MODE, int MAXT>
 cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
-    constexpr int NIN = (MODE == kGated) ? 2 : 1;
+    constexpr int NIN = fwd_inputs(MODE);
     constexpr int R = fwd_rows<VPT>();
     const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
     const size_t fixed = 2 * R * 32 * 4;
@@ -601,7 +620,7 @@ cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
 
 template <int VPT, int MODE, int MAXT>
 cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
-    constexpr int NIN = (MODE == kPlain) ? 2 : 3;
+    constexpr int NIN = bwd_inputs(MODE);
     constexpr int R = bwd_rows<VPT, MAXT>();
     const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
     const size_t fixed = 2 * R * 32 * 4;
@@ -649,6 +668,8 @@ cudaError_t launch_wide_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStrea
         case kPlain: return fwd_dispatch<kPlain>(a, c, st);
         case kResidual: return fwd_dispatch<kResidual>(a, c, st);
         case kGated: return fwd_dispatch<kGated>(a, c, st);
+        case kFusedAdd:
+        case kFusedAddNoGres: return fwd_dispatch<kFusedAdd>(a, c, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -658,6 +679,8 @@ cudaError_t launch_wide_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStrea
         case kPlain: return bwd_dispatch<kPlain>(a, c, st);
         case kResidual: return bwd_dispatch<kResidual>(a, c, st);
         case kGated: return bwd_dispatch<kGated>(a, c, st);
+        case kFusedAdd: return bwd_dispatch<kFusedAdd>(a, c, st);
+        case kFusedAddNoGres: return bwd_dispatch<kFusedAddNoGres>(a, c, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -26,7 +26,7 @@ def chunk_rows_hint(T, D):
     return T if n <= 1 else -(-T // (n - 1)) - 1, n
 
 
-def run_fwd(variant, x, w, eps, zc, z=None, ld_out=None):
+def run_fwd(variant, x, w, eps, zc, z=None, ld_out=None, res=None):
     T, D = x.shape
     y = empty_act(T, D, ld_out)
     rstd = torch.empty(T, dtype=torch.float32, device=DEV)
@@ -39,12 +39,16 @@ def run_fwd(variant, x, w, eps, zc, z=None, ld_out=None):
         out["x_copy"] = xc
     elif variant == "gated":
         rn.rmsnorm_gated_fwd(x, z, w, y, rstd, eps, zc)
+    elif variant == "fused":
+        ro = empty_act(T, D, ld_out)
+        rn.rmsnorm_fused_add_fwd(x, res, w, y, rstd, ro, eps, zc)
+        out["res_out"] = ro
     else:
         raise ValueError(variant)
     return out
 
 
-def run_bwd(variant, g, x, w, rstd, zc, z=None, g_res=None, ld_out=None, split=False):
+def run_bwd(variant, g, x, w, rstd, zc, z=None, g_res=None, ld_out=None, split=False, res=None):
     T, D = x.shape
     dx = empty_act(T, D, ld_out)
     dg = torch.empty(D, dtype=torch.float32, device=DEV)
@@ -59,12 +63,17 @@ def run_bwd(variant, g, x, w, rstd, zc, z=None, g_res=None, ld_out=None, split=F
         dz = empty_act(T, D, ld_out)
         rn.rmsnorm_gated_bwd(g, x, z, w, rstd, dx, dz, target, ws, zc)
         out["dz"] = dz
+    elif variant == "fused":
+        rn.rmsnorm_fused_add_bwd(g, x, res, w, rstd, g_res, dx, target, ws, zc)
     if split:
         rn.rmsnorm_dgamma_reduce(ws, T, D, dg)
     return out
 
 
-def oracle_fwd(variant, x, w, eps, zc, z=None):
+def oracle_fwd(variant, x, w, eps, zc, z=None, res=None):
+    if variant == "fused":
+        y, r, ro = oracle.fused_add_fwd(to_f64(x), to_f64(res), to_f64(w), eps, zc)
+        return y, r
     if variant == "gated":
         y, r = oracle.gated_fwd(to_f64(x), to_f64(z), to_f64(w), eps, zc)
     else:
@@ -72,20 +81,27 @@ def oracle_fwd(variant, x, w, eps, zc, z=None):
     return y, r
 
 
-def check_fwd(variant, x, w, eps, zc, out, z=None, name=""):
-    y_ref, r_ref = oracle_fwd(variant, x, w, eps, zc, z)
+def check_fwd(variant, x, w, eps, zc, out, z=None, name="", res=None):
+    y_ref, r_ref = oracle_fwd(variant, x, w, eps, zc, z, res)
     assert_rel(f"{name} rstd", to_f64(out["rstd"]), r_ref, 1e-5)
     assert_bf16_parity(f"{name} y", to_f64(out["y"]), y_ref)
+    if variant == "fused":
+        _, _, ro = oracle.fused_add_fwd(to_f64(x), to_f64(res), to_f64(w), eps, zc)
+        np.testing.assert_array_equal(to_f64(out["res_out"]), ro, err_msg=f"{name} res_out")
     if variant == "residual":
         assert torch.equal(out["x_copy"].view(torch.int16), x.view(torch.int16)), f"{name} x_copy"
 
 
-def check_bwd(variant, g, x, w, rstd, zc, out, z=None, g_res=None, name=""):
+def check_bwd(variant, g, x, w, rstd, zc, out, z=None, g_res=None, name="", res=None):
     """Compare against the oracle run with the same saved rstd. Returns the number
     of elements accepted by the cancellation clause (dx, dz, dgamma)."""
     T, D = x.shape
     r64 = to_f64(rstd)
-    if variant == "gated":
+    if variant == "fused":
+        gr = None if g_res is None else to_f64(g_res)
+        dx_ref, dw_ref, diag = oracle.fused_add_bwd(to_f64(g), to_f64(x), to_f64(res), to_f64(w), r64, gr, zc,
+                                                    diagnostics=True)
+    elif variant == "gated":
         dx_ref, dz_ref, dw_ref, diag = oracle.gated_bwd(to_f64(g), to_f64(x), to_f64(z), to_f64(w), r64, zc,
                                                         diagnostics=True)
     else:
