@@ -154,6 +154,29 @@ int rmsnorm_fused_add_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, i
                           void* ws, size_t ws_bytes,
                           int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
 
+/* Backward with recomputation of the forward output (activation recompute):
+ * exactly rmsnorm_residual_bwd (g_res NULL = the plain / zero-centred
+ * backward) that also writes y [T][ldy] = bf16((x * rstd) * w_eff) from the
+ * saved rstd — the same operations as the forward, so the same bits as the
+ * forward's y — in the same pass over x, for one extra row write instead of a
+ * second forward launch. */
+int rmsnorm_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                          const float* w, const float* rstd,
+                          const rmsn_bf16* g_res, int64_t ldgr,
+                          rmsn_bf16* dx, int64_t lddx, float* dgamma,
+                          rmsn_bf16* y, int64_t ldy,
+                          void* ws, size_t ws_bytes,
+                          int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
+/* Gated backward with recomputation of the gated forward output y (same bits
+ * as rmsnorm_gated_fwd's y); otherwise exactly rmsnorm_gated_bwd. */
+int rmsnorm_gated_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                                const rmsn_bf16* z, int64_t ldz, const float* w, const float* rstd,
+                                rmsn_bf16* dx, int64_t lddx, rmsn_bf16* dz, int64_t lddz, float* dw,
+                                rmsn_bf16* y, int64_t ldy,
+                                void* ws, size_t ws_bytes,
+                                int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
 /* Weight-gradient pass 2 on its own: sums the per-chunk partials that a backward
  * call with a NULL dgamma/dw left in ws (same T, D and workspace), in the fixed
  * order, into dgamma [D]. ws must be unchanged since that call. */

@@ -29,14 +29,15 @@ __all__ = [
     "rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
     "rmsnorm_gated_fwd", "rmsnorm_gated_bwd", "rmsnorm_dgamma_reduce",
     "rmsnorm_bwd_workspace_bytes", "rmsnorm_status_string", "rmsnorm_device_error",
-    "rmsnorm_bwd_noalloc", "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "EXPORTED_SYMBOLS",
+    "rmsnorm_bwd_noalloc", "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_bwd_recompute",
+    "rmsnorm_gated_bwd_recompute", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
     "rmsnorm_status_string", "rmsnorm_fwd", "rmsnorm_bwd_workspace_bytes", "rmsnorm_bwd",
     "rmsnorm_residual_fwd", "rmsnorm_residual_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
     "rmsnorm_dgamma_reduce", "rmsnorm_device_error", "rmsnorm_bwd_noalloc",
-    "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd",
+    "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_bwd_recompute", "rmsnorm_gated_bwd_recompute",
 )
 
 _P = ctypes.c_void_p
@@ -62,6 +63,10 @@ _SIGS = {
     "rmsnorm_fused_add_fwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _I64, _P, _P, _I64, _I64, _I64, _F, _INT, _P]),
     "rmsnorm_fused_add_bwd": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _SZ,
                                      _I64, _I64, _INT, _P]),
+    "rmsnorm_bwd_recompute": (_INT, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64, _P, _SZ,
+                                     _I64, _I64, _INT, _P]),
+    "rmsnorm_gated_bwd_recompute": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64,
+                                           _P, _SZ, _I64, _I64, _INT, _P]),
 }
 
 _lock = threading.Lock()
@@ -253,6 +258,38 @@ def rmsnorm_fused_add_bwd(g, x, res, w, rstd, g_res, dh, dgamma, ws, zero_center
     _check("rmsnorm_fused_add_bwd", load().rmsnorm_fused_add_bwd(
         _ptr(g), ldg, _ptr(x), ldx, _ptr(res), ldr, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dh), ldd,
         _ptr(dgamma), wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_bwd_recompute(g, x, w, rstd, g_res, dx, dgamma, y, ws, zero_centered_gamma: bool = False,
+                          stream=None):
+    """rmsnorm_residual_bwd (``g_res`` may be None) that also writes the forward's y."""
+    T, D = x.shape
+    ldg, ldx, lddx, ldy = _act(g, "g", T, D), _act(x, "x", T, D), _act(dx, "dx", T, D), _act(y, "y", T, D)
+    ldgr = _act(g_res, "g_res", T, D) if g_res is not None else D
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_bwd_recompute", load().rmsnorm_bwd_recompute(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dx), lddx, _ptr(dgamma),
+        _ptr(y), ldy, wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_bwd_recompute(g, x, z, w, rstd, dx, dz, dw, y, ws, zero_centered_gamma: bool = True,
+                                stream=None):
+    """rmsnorm_gated_bwd that also writes the gated forward's y."""
+    T, D = x.shape
+    ldg, ldx, ldz = _act(g, "g", T, D), _act(x, "x", T, D), _act(z, "z", T, D)
+    lddx, lddz, ldy = _act(dx, "dx", T, D), _act(dz, "dz", T, D), _act(y, "y", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dw is not None:
+        _f32(dw, "dw", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_gated_bwd_recompute", load().rmsnorm_gated_bwd_recompute(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dz), lddz, _ptr(dw),
+        _ptr(y), ldy, wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
 
 
 def rmsnorm_dgamma_reduce(ws, T: int, D: int, dgamma, stream=None):

@@ -355,6 +355,51 @@ int rmsnorm_fused_add_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, i
     return run_bwd(g_res ? kFusedAdd : kFusedAddNoGres, a, dgamma, stream);
 }
 
+int rmsnorm_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
+                          const float* rstd, const rmsn_bf16* g_res, int64_t ldgr, rmsn_bf16* dx, int64_t lddx,
+                          float* dgamma, rmsn_bf16* y, int64_t ldy, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                          int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.y = y; a.ldy = ldy; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(g_res ? kResidual : kPlain, a, dgamma, stream);
+}
+
+int rmsnorm_gated_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z,
+                                int64_t ldz, const float* w, const float* rstd, rmsn_bf16* dx, int64_t lddx,
+                                rmsn_bf16* dz, int64_t lddz, float* dw, rmsn_bf16* y, int64_t ldy, void* ws,
+                                size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_act(dz, lddz, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dw) RMSN_TRY(check_vec(dw));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.dz = dz; a.lddz = lddz; a.y = y; a.ldy = ldy; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(kGated, a, dw, stream);
+}
+
 int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D, float* dgamma,
                           rmsn_stream stream) {
     RMSN_TRY(check_shape(T, D));

@@ -45,6 +45,7 @@ struct BwdArgs {
     uint16_t* dx; int64_t lddx;
     uint16_t* dz; int64_t lddz;         // gated
     float* partials;                    // [nchunks][D] fp32 (workspace)
+    uint16_t* y; int64_t ldy;           // optional: the forward output, recomputed (null = skip)
     int64_t T; int D; int zc;
     float inv_d_pow2;                   // 1/D if D is a power of two, else 0
 };

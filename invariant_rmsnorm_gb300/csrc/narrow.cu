@@ -431,14 +431,22 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 }
                 st_global_cs(a.dx + row * a.lddx + 8 * l, pack8(o));
                 if (MODE == kGated) {
-                    float dzv[8];
+                    float dzv[8], yv[8];
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
                         const float u = fmul(fmul(xf[e], r), we[e]);
                         const float dsilu = fmul(sg[e], fadd(1.0f, fmul(tf[e], fsub(1.0f, sg[e]))));
                         dzv[e] = fmul(fmul(g0[e], u), dsilu);
+                        yv[e] = fmul(u, fmul(tf[e], sg[e]));
                     }
                     st_global_cs(a.dz + row * a.lddz + 8 * l, pack8(dzv));
+                    if (a.y) st_global_cs(a.y + row * a.ldy + 8 * l, pack8(yv));
+                } else if (a.y) {
+                    // The forward output again, from the saved rstd (same bits as the forward).
+                    float yv[8];
+#pragma unroll
+                    for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xf[e], r), we[e]);
+                    st_global_cs(a.y + row * a.ldy + 8 * l, pack8(yv));
                 }
             }
         }

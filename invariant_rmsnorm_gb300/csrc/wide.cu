@@ -547,7 +547,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         }
                         st_global_cs(dxrow + 8 * v, pack8(o));
                         if (MODE == kGated) {
-                            float dzv[8];
+                            float dzv[8], yv[8];
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
                                 const float z = tz[r][j][e];
@@ -555,8 +555,17 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                 const float u = fmul(fmul(xs[r][j][e], r1), we[j][e]);
                                 const float dsilu = fmul(sg, fadd(1.0f, fmul(z, fsub(1.0f, sg))));
                                 dzv[e] = fmul(fmul(g0[r][j][e], u), dsilu);
+                                yv[e] = fmul(u, fmul(z, sg));
                             }
                             st_global_cs(a.dz + row * a.lddz + 8 * v, pack8(dzv));
+                            if (a.y) st_global_cs(a.y + row * a.ldy + 8 * v, pack8(yv));
+                        } else if (a.y) {
+                            // The forward output again, from the saved rstd: same operations,
+                            // same bits as the forward's y.
+                            float yv[8];
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), we[j][e]);
+                            st_global_cs(a.y + row * a.ldy + 8 * v, pack8(yv));
                         }
                     }
                 }

@@ -1,0 +1,54 @@
+"""Backward with recomputation of the forward output (SURVEY's "single pass
+for recompute" row): the y it writes is the forward's y bit for bit, and its
+dx / dz / dgamma are those of the plain backward bit for bit."""
+from __future__ import annotations
+
+import pytest
+import torch
+
+import invariant_rmsnorm_gb300 as rn
+from invariant_rmsnorm_gb300 import synth
+from tests.gpu_common import DEV, empty_act, run_bwd, run_fwd
+
+pytestmark = pytest.mark.gpu
+
+
+def _bits(t):
+    return t.contiguous().view(torch.int16)
+
+
+@pytest.mark.parametrize("with_gres", [False, True])
+@pytest.mark.parametrize("zc", [False, True])
+@pytest.mark.parametrize("D,T", [(128, 333), (200, 70), (2048, 333), (4096, 1000), (7168, 70)])
+def test_bwd_recompute_matches_forward_and_backward(D, T, zc, with_gres):
+    x = synth.normal_bf16((T, D), D, DEV)
+    g = synth.normal_bf16((T, D), D + 1, DEV)
+    gr = synth.normal_bf16((T, D), D + 2, DEV) if with_gres else None
+    w = synth.gamma_f32(D, D + 3, DEV, mean=0.0 if zc else 1.0, std=0.1)
+    fo = run_fwd("plain", x, w, 1e-6, zc)
+    ref = run_bwd("residual" if with_gres else "plain", g, x, w, fo["rstd"], zc, g_res=gr)
+    dx, dg = torch.empty_like(x), torch.empty(D, device=DEV)
+    y = empty_act(T, D, D + 8)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=DEV)
+    rn.rmsnorm_bwd_recompute(g, x, w, fo["rstd"], gr, dx, dg, y, ws, zc)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y), _bits(fo["y"]))
+    assert torch.equal(_bits(dx), _bits(ref["dx"]))
+    assert torch.equal(dg.view(torch.int32), ref["dgamma"].view(torch.int32))
+
+
+@pytest.mark.parametrize("D,T", [(128, 1000), (2048, 70)])
+def test_gated_bwd_recompute_matches_forward_and_backward(D, T):
+    x = synth.normal_bf16((T, D), 1, DEV)
+    z = synth.normal_bf16((T, D), 2, DEV)
+    g = synth.normal_bf16((T, D), 3, DEV)
+    w = synth.gamma_f32(D, 4, DEV, mean=0.0, std=0.1)
+    fo = run_fwd("gated", x, w, 1e-6, True, z=z)
+    ref = run_bwd("gated", g, x, w, fo["rstd"], True, z=z)
+    dx, dz, dw, y = torch.empty_like(x), torch.empty_like(x), torch.empty(D, device=DEV), torch.empty_like(x)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=DEV)
+    rn.rmsnorm_gated_bwd_recompute(g, x, z, w, fo["rstd"], dx, dz, dw, y, ws, True)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y), _bits(fo["y"]))
+    assert torch.equal(_bits(dx), _bits(ref["dx"])) and torch.equal(_bits(dz), _bits(ref["dz"]))
+    assert torch.equal(dw.view(torch.int32), ref["dgamma"].view(torch.int32))
