@@ -40,7 +40,7 @@ from . import build as _build
 __all__ = [
     "round_bf16", "num_threads",
     "rmsnorm_fwd", "rmsnorm_bwd", "residual_fwd", "residual_bwd",
-    "gated_fwd", "gated_bwd", "weight_grad", "fused_add_fwd", "fused_add_bwd",
+    "gated_fwd", "gated_bwd", "weight_grad", "fused_add_fwd", "fused_add_bwd", "gated_hf_fwd",
 ]
 
 _lock = threading.Lock()
@@ -65,6 +65,8 @@ def _load():
             lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
                                           _D, _D, _D, _D, _D]
             lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D, _D]
+            lib.orc_gated_hf_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
+            lib.orc_gated_hf_fwd.restype = None
             lib.orc_fused_add_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D, _D]
             lib.orc_fused_add_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
                                               _D, _D, _D]
@@ -249,3 +251,17 @@ def fused_add_bwd(g, x, res, w, rstd, g_res=None, zero_centered_gamma: bool = Fa
                               int(rounded), _p(dh), _p(dw), _p(hs), _p(diag.get("dx_pre")),
                               _p(diag.get("dx_scale")), _p(diag.get("dw_abs")))
     return (dh, dw, diag) if diagnostics else (dh, dw)
+
+
+def gated_hf_fwd(x, z, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+    """Gated forward in the HF/transformers convention (normalised value and weight
+    multiply in bf16). Returns ``(y, rstd)``."""
+    x = _arr(x)
+    T, D = x.shape
+    z = _arr(z, (T, D))
+    w = _arr(w, (D,))
+    y = np.empty((T, D))
+    rstd = np.empty((T,))
+    _load().orc_gated_hf_fwd(T, D, _p(x), _p(z), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
+                             int(rounded), _p(y), _p(rstd))
+    return y, rstd

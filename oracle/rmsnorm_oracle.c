@@ -274,3 +274,29 @@ void orc_fused_add_bwd(int64_t T, int64_t D, const double* g, const double* x, c
     orc_rmsnorm_bwd(T, D, g, h_scratch, w, rstd, g_res, zero_centered, rounded, dh, dw, dh_pre, dh_scale,
                     dw_abs);
 }
+
+/* ------------------------------------------------------------------------ */
+/* Gated norm, HF/transformers convention, forward only ([ZC-norm]: the two  */
+/* upstreams round the gated norm differently; the vLLM one multiplies by    */
+/* the weight in fp32, and with fp32 inputs the two agree bitwise because    */
+/* "the cast" is then a no-op). Reading: the normalised value is cast to the */
+/* activation dtype (bf16) and the weight multiply happens in that dtype:    */
+/*   n = bf16(fl32(x r));  t = bf16(fl32(bf16(w_eff) n));  y = bf16(t silu(z)) */
+/* In unrounded mode every cast is the identity, so the function equals the  */
+/* vLLM convention's.                                                        */
+/* ------------------------------------------------------------------------ */
+void orc_gated_hf_fwd(int64_t T, int64_t D, const double* x, const double* z, const double* w,
+                      double eps, int zero_centered, int rounded, double* y, double* rstd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) {
+        const double* xr = x + t * D;
+        double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);
+        rstd[t] = r;
+        for (int64_t j = 0; j < D; ++j) {
+            double n = maybe_bf16(maybe_fl32(xr[j] * r, rounded), rounded);
+            double wb = maybe_bf16(w_eff(w[j], zero_centered, rounded), rounded);
+            double tt = maybe_bf16(maybe_fl32(wb * n, rounded), rounded);
+            y[t * D + j] = maybe_bf16(tt * silu(z[t * D + j]), rounded);
+        }
+    }
+}

@@ -384,3 +384,46 @@ def test_fused_add_rounding_bruteforce(zc):
     np.testing.assert_array_equal(y0, yp)
     np.testing.assert_array_equal(r0, rp)
     np.testing.assert_array_equal(ro0, x)
+
+
+# ==========================================================================
+# Gated norm, HF convention (witness of the convention divergence)
+# ==========================================================================
+
+def test_gated_hf_convention_divergence_matches_the_pages():
+    """bf16, D=128, 512 rows, randn weights: the HF and vLLM conventions agree on
+    roughly two thirds of the elements and differ by at most a few bf16 ulps of
+    values near 10 (the page: 65 %, max |d| 6.25e-2); with no rounding at all
+    (the fp32-input case, where the casts are no-ops) they are identical."""
+    gold = _golden("zc_norm_gated_conventions.json")
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(gold["rows"], gold["D"], generator=g).to(torch.bfloat16).double().numpy()
+    z = torch.randn(gold["rows"], gold["D"], generator=g).to(torch.bfloat16).double().numpy()
+    w = np.float32(torch.randn(gold["D"], generator=g).double().numpy()).astype(np.float64)
+    yv, rv = oracle.gated_fwd(x, z, w, 1e-6, zero_centered_gamma=False)
+    yh, rh = oracle.gated_hf_fwd(x, z, w, 1e-6, zero_centered_gamma=False)
+    np.testing.assert_array_equal(rv, rh)
+    same = float(np.mean(yv == yh))
+    mx = float(np.abs(yv - yh).max())
+    assert abs(same - gold["same_fraction"]) < 0.15, same
+    assert gold["max_abs_diff"] / 2 <= mx <= 2 * gold["max_abs_diff"], mx
+    ye, _ = oracle.gated_fwd(x, z, w, 1e-6, zero_centered_gamma=False, rounded=False)
+    yhe, _ = oracle.gated_hf_fwd(x, z, w, 1e-6, zero_centered_gamma=False, rounded=False)
+    np.testing.assert_array_equal(ye, yhe)
+
+
+def test_gated_hf_rounding_points_bruteforce():
+    """Each of the HF reading's casts, checked with rationals and the bf16 table."""
+    T, D = 2, 16
+    x = _bf16_grid(RNG.standard_normal((T, D)))
+    z = _bf16_grid(RNG.standard_normal((T, D)))
+    w = np.float32(RNG.standard_normal(D)).astype(np.float64)
+    y, r = oracle.gated_hf_fwd(x, z, w, 1e-6)
+    for t in range(T):
+        for j in range(D):
+            n = bf16_round_bruteforce(Fraction(float(np.float32(Fraction(x[t, j]) * Fraction(r[t])))))
+            wb = bf16_round_bruteforce(Fraction(w[j]))
+            tt = bf16_round_bruteforce(Fraction(float(np.float32(Fraction(wb) * Fraction(n)))))
+            silu = z[t, j] / (1.0 + math.exp(-z[t, j]))
+            assert abs(y[t, j] - bf16_round_bruteforce(Fraction(tt) * Fraction(silu))) <= \
+                abs(y[t, j]) * 2.0**-40  # silu rounded to double only
