@@ -121,6 +121,16 @@ int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64
                       int64_t T, int64_t D, float eps, int zero_centered_gamma,
                       rmsn_stream stream);
 
+/* Gated forward in the HF/transformers convention, kept as a witness of the
+ * convention divergence ([ZC-norm]: the two upstreams round the gated norm
+ * differently; they agree bitwise with fp32 inputs). Forward only:
+ *   n = bf16((x * r)),  t = bf16(bf16(w_eff) * n),  y = bf16(t * silu(z)).
+ * Arguments as rmsnorm_gated_fwd. */
+int rmsnorm_gated_hf_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz,
+                         const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
+                         int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                         rmsn_stream stream);
+
 /* Gated backward: with q = silu(z) and u = (x r) w_eff,
  *   dx = plain backward with g*q in place of g;  dz = bf16( g u silu'(z) );
  *   dw_j = sum_t g q x r. dw NULL: as rmsnorm_bwd with dgamma NULL. */

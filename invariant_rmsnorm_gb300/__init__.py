@@ -30,7 +30,7 @@ __all__ = [
     "rmsnorm_gated_fwd", "rmsnorm_gated_bwd", "rmsnorm_dgamma_reduce",
     "rmsnorm_bwd_workspace_bytes", "rmsnorm_status_string", "rmsnorm_device_error",
     "rmsnorm_bwd_noalloc", "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_bwd_recompute",
-    "rmsnorm_gated_bwd_recompute", "EXPORTED_SYMBOLS",
+    "rmsnorm_gated_bwd_recompute", "rmsnorm_gated_hf_fwd", "EXPORTED_SYMBOLS",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -38,6 +38,7 @@ EXPORTED_SYMBOLS = (
     "rmsnorm_residual_fwd", "rmsnorm_residual_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
     "rmsnorm_dgamma_reduce", "rmsnorm_device_error", "rmsnorm_bwd_noalloc",
     "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_bwd_recompute", "rmsnorm_gated_bwd_recompute",
+    "rmsnorm_gated_hf_fwd",
 )
 
 _P = ctypes.c_void_p
@@ -55,6 +56,7 @@ _SIGS = {
     "rmsnorm_residual_bwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _SZ,
                                     _I64, _I64, _INT, _P]),
     "rmsnorm_gated_fwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _F, _INT, _P]),
+    "rmsnorm_gated_hf_fwd": (_INT, [_P, _I64, _P, _I64, _P, _P, _I64, _P, _I64, _I64, _F, _INT, _P]),
     "rmsnorm_gated_bwd": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P,
                                  _SZ, _I64, _I64, _INT, _P]),
     "rmsnorm_dgamma_reduce": (_INT, [_P, _SZ, _I64, _I64, _P, _P]),
@@ -183,6 +185,17 @@ def rmsnorm_gated_fwd(x, z, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: 
     _f32(w, "w", D)
     _f32(rstd, "rstd", T)
     _check("rmsnorm_gated_fwd", load().rmsnorm_gated_fwd(
+        _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(y), ldy, _ptr(rstd), T, D, float(eps),
+        int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_hf_fwd(x, z, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: bool = False, stream=None):
+    """Gated forward in the HF convention (bf16 casts around the weight multiply)."""
+    T, D = x.shape
+    ldx, ldz, ldy = _act(x, "x", T, D), _act(z, "z", T, D), _act(y, "y", T, D)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_gated_hf_fwd", load().rmsnorm_gated_hf_fwd(
         _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(y), ldy, _ptr(rstd), T, D, float(eps),
         int(zero_centered_gamma), _stream(stream, x.device)))
 

@@ -252,6 +252,23 @@ int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64
     return run_fwd(kGated, a, stream);
 }
 
+int rmsnorm_gated_hf_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz, const float* w,
+                         rmsn_bf16* y, int64_t ldy, float* rstd, int64_t T, int64_t D, float eps,
+                         int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kGatedHF, a, stream);
+}
+
 int rmsnorm_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
                 const float* rstd, rmsn_bf16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes,
                 int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {

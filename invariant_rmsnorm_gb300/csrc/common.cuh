@@ -210,6 +210,9 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// An fp32 value rounded to bf16 (nearest even) and widened back.
+__device__ __forceinline__ float round_bf16f(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
+
 // ---------------------------------------------------------------------------
 // Separately rounded fp32 arithmetic (never contracted into FMA).
 // ---------------------------------------------------------------------------

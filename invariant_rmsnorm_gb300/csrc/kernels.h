@@ -10,14 +10,18 @@ namespace rmsn {
 
 // kFusedAdd / kFusedAddNoGres: the norm of h = x + res (fp32), forward also
 // returning bf16(h); the backward with or without the gradient of that output.
-enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2, kFusedAdd = 3, kFusedAddNoGres = 4 };
+// kGatedHF: the gated forward in the HF convention (bf16 casts around the
+// weight multiply); forward only.
+enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2, kFusedAdd = 3, kFusedAddNoGres = 4, kGatedHF = 5 };
+
+__host__ __device__ constexpr bool is_fused(int mode) { return mode == kFusedAdd || mode == kFusedAddNoGres; }
+__host__ __device__ constexpr bool is_gated(int mode) { return mode == kGated || mode == kGatedHF; }
 
 // Operands streamed per row, by mode.
-__host__ __device__ constexpr int fwd_inputs(int mode) { return (mode == kGated || mode >= kFusedAdd) ? 2 : 1; }
+__host__ __device__ constexpr int fwd_inputs(int mode) { return (is_gated(mode) || is_fused(mode)) ? 2 : 1; }
 __host__ __device__ constexpr int bwd_inputs(int mode) {
     return mode == kPlain ? 2 : (mode == kResidual || mode == kGated || mode == kFusedAddNoGres) ? 3 : 4;
 }
-__host__ __device__ constexpr bool is_fused(int mode) { return mode >= kFusedAdd; }
 __host__ __device__ constexpr bool has_gres(int mode) { return mode == kResidual || mode == kFusedAdd; }
 
 // Everything a forward launch needs (unused pointers are null).

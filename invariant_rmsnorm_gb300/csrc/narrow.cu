@@ -278,6 +278,16 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
                             const float q = fmul(zf[e], sigmoidf_rn(zf[e]));
                             o[e] = fmul(fmul(fmul(f[e], r), we[e]), q);
                         }
+                    } else if (MODE == kGatedHF) {
+                        // HF convention: normalised value and weight multiply in bf16.
+                        float zf[8];
+                        unpack8(zv, zf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            const float n = round_bf16f(fmul(f[e], r));
+                            const float t = round_bf16f(fmul(round_bf16f(we[e]), n));
+                            o[e] = fmul(t, fmul(zf[e], sigmoidf_rn(zf[e])));
+                        }
                     } else {
 #pragma unroll
                         for (int e = 0; e < 8; ++e) o[e] = fmul(fmul(f[e], r), we[e]);
@@ -500,7 +510,7 @@ cudaError_t nfwd_t(const FwdArgs& a, cudaStream_t st) {
     NarrowMaps m;
     std::memset(&m, 0, sizeof(m));
     cudaError_t e = encode_rows_2d(&m.a, a.x, a.T, a.D, a.ldx, RS);
-    if (e == cudaSuccess && MODE == kGated) e = encode_rows_2d(&m.b, a.z, a.T, a.D, a.ldz, RS);
+    if (e == cudaSuccess && is_gated(MODE)) e = encode_rows_2d(&m.b, a.z, a.T, a.D, a.ldz, RS);
     if (e == cudaSuccess && is_fused(MODE)) e = encode_rows_2d(&m.b, a.res, a.T, a.D, a.ldres, RS);
     if (e != cudaSuccess) return e;
     const size_t stage = static_cast<size_t>(NIN) * RS * a.D * 2;
@@ -609,6 +619,7 @@ cudaError_t launch_narrow_fwd(Mode md, const FwdArgs& a, const RowCfg& c, cudaSt
         case kGated: return nfwd_dispatch<kGated>(a, c, st);
         case kFusedAdd:
         case kFusedAddNoGres: return nfwd_dispatch<kFusedAdd>(a, c, st);
+        case kGatedHF: return nfwd_dispatch<kGatedHF>(a, c, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -620,6 +631,7 @@ cudaError_t launch_narrow_bwd(Mode md, const BwdArgs& a, const RowCfg& c, cudaSt
         case kGated: return nbwd_dispatch<kGated>(a, c, st);
         case kFusedAdd: return nbwd_dispatch<kFusedAdd>(a, c, st);
         case kFusedAddNoGres: return nbwd_dispatch<kFusedAddNoGres>(a, c, st);
+        default: break;
     }
     return cudaErrorInvalidValue;
 }

@@ -244,7 +244,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                     const int64_t row = cta + static_cast<int64_t>(i * R + r) * G;
                     unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
                     bulk_g2s(dst, a.x + row * a.ldx, row_bytes, &full[s], pol);
-                    if (MODE == kGated) bulk_g2s(dst + row_bytes, a.z + row * a.ldz, row_bytes, &full[s], pol);
+                    if (is_gated(MODE)) bulk_g2s(dst + row_bytes, a.z + row * a.ldz, row_bytes, &full[s], pol);
                     if (is_fused(MODE)) bulk_g2s(dst + row_bytes, a.res + row * a.ldres, row_bytes, &full[s], pol);
                 }
             });
@@ -327,6 +327,16 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
                             for (int e = 0; e < 8; ++e) {
                                 const float q = fmul(zf[e], sigmoidf_rn(zf[e]));
                                 o[e] = fmul(fmul(fmul(f[e], rr), we[j][e]), q);
+                            }
+                        } else if (MODE == kGatedHF) {
+                            // HF convention: normalised value and weight multiply in bf16.
+                            float zf[8];
+                            unpack8(zv[r][j], zf);
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                const float n = round_bf16f(fmul(f[e], rr));
+                                const float t = round_bf16f(fmul(round_bf16f(we[j][e]), n));
+                                o[e] = fmul(t, fmul(zf[e], sigmoidf_rn(zf[e])));
                             }
                         } else {
 #pragma unroll
@@ -679,6 +689,7 @@ cudaError_t launch_wide_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStrea
         case kGated: return fwd_dispatch<kGated>(a, c, st);
         case kFusedAdd:
         case kFusedAddNoGres: return fwd_dispatch<kFusedAdd>(a, c, st);
+        case kGatedHF: return fwd_dispatch<kGatedHF>(a, c, st);
     }
     return cudaErrorInvalidValue;
 }
@@ -690,6 +701,7 @@ cudaError_t launch_wide_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStrea
         case kGated: return bwd_dispatch<kGated>(a, c, st);
         case kFusedAdd: return bwd_dispatch<kFusedAdd>(a, c, st);
         case kFusedAddNoGres: return bwd_dispatch<kFusedAddNoGres>(a, c, st);
+        default: break;
     }
     return cudaErrorInvalidValue;
 }

@@ -41,6 +41,7 @@ __all__ = [
     "round_bf16", "num_threads",
     "rmsnorm_fwd", "rmsnorm_bwd", "residual_fwd", "residual_bwd",
     "gated_fwd", "gated_bwd", "weight_grad", "fused_add_fwd", "fused_add_bwd", "gated_hf_fwd",
+    "gated_hf_apply",
 ]
 
 _lock = threading.Lock()
@@ -67,6 +68,8 @@ def _load():
             lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D, _D]
             lib.orc_gated_hf_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
             lib.orc_gated_hf_fwd.restype = None
+            lib.orc_gated_hf_apply.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _INT, _D]
+            lib.orc_gated_hf_apply.restype = None
             lib.orc_fused_add_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D, _D]
             lib.orc_fused_add_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
                                               _D, _D, _D]
@@ -265,3 +268,16 @@ def gated_hf_fwd(x, z, w, eps: float, zero_centered_gamma: bool = False, rounded
     _load().orc_gated_hf_fwd(T, D, _p(x), _p(z), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
                              int(rounded), _p(y), _p(rstd))
     return y, rstd
+
+
+def gated_hf_apply(x, z, w, rstd, zero_centered_gamma: bool = False, rounded: bool = True):
+    """The HF-convention gated output for given inverse RMS values (the second half
+    of ``gated_hf_fwd``). Returns ``y``."""
+    x = _arr(x)
+    T, D = x.shape
+    z = _arr(z, (T, D))
+    w = _arr(w, (D,))
+    rstd = _arr(rstd, (T,))
+    y = np.empty((T, D))
+    _load().orc_gated_hf_apply(T, D, _p(x), _p(z), _p(w), _p(rstd), int(zero_centered_gamma), int(rounded), _p(y))
+    return y

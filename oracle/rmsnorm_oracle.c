@@ -285,18 +285,24 @@ void orc_fused_add_bwd(int64_t T, int64_t D, const double* g, const double* x, c
 /* In unrounded mode every cast is the identity, so the function equals the  */
 /* vLLM convention's.                                                        */
 /* ------------------------------------------------------------------------ */
-void orc_gated_hf_fwd(int64_t T, int64_t D, const double* x, const double* z, const double* w,
-                      double eps, int zero_centered, int rounded, double* y, double* rstd) {
+/* The HF convention's output for given fp32 inverse RMS values. */
+void orc_gated_hf_apply(int64_t T, int64_t D, const double* x, const double* z, const double* w,
+                        const double* rstd, int zero_centered, int rounded, double* y) {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
-        const double* xr = x + t * D;
-        double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);
-        rstd[t] = r;
+        const double r = rstd[t];
         for (int64_t j = 0; j < D; ++j) {
-            double n = maybe_bf16(maybe_fl32(xr[j] * r, rounded), rounded);
+            double n = maybe_bf16(maybe_fl32(x[t * D + j] * r, rounded), rounded);
             double wb = maybe_bf16(w_eff(w[j], zero_centered, rounded), rounded);
             double tt = maybe_bf16(maybe_fl32(wb * n, rounded), rounded);
             y[t * D + j] = maybe_bf16(tt * silu(z[t * D + j]), rounded);
         }
     }
+}
+
+void orc_gated_hf_fwd(int64_t T, int64_t D, const double* x, const double* z, const double* w,
+                      double eps, int zero_centered, int rounded, double* y, double* rstd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < T; ++t) rstd[t] = maybe_fl32(row_inv_rms(x + t * D, D, eps), rounded);
+    orc_gated_hf_apply(T, D, x, z, w, rstd, zero_centered, rounded, y);
 }

@@ -427,3 +427,11 @@ def test_gated_hf_rounding_points_bruteforce():
             silu = z[t, j] / (1.0 + math.exp(-z[t, j]))
             assert abs(y[t, j] - bf16_round_bruteforce(Fraction(tt) * Fraction(silu))) <= \
                 abs(y[t, j]) * 2.0**-40  # silu rounded to double only
+
+
+def test_gated_hf_apply_is_the_forward_given_its_rstd():
+    x = _bf16_grid(RNG.standard_normal((4, 32)))
+    z = _bf16_grid(RNG.standard_normal((4, 32)))
+    w = np.float32(RNG.standard_normal(32)).astype(np.float64)
+    y, r = oracle.gated_hf_fwd(x, z, w, 1e-6, zero_centered_gamma=True)
+    np.testing.assert_array_equal(oracle.gated_hf_apply(x, z, w, r, zero_centered_gamma=True), y)
