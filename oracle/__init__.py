@@ -11,9 +11,12 @@ row-major ``[T, D]`` for activations, ``[D]`` for the weight and ``[T]`` for the
 inverse RMS. Callers convert bf16 tensors to float64 exactly before calling.
 
 ``rounded=True`` applies the method's rounding points (fp32 inverse RMS and
-weight gradient, fp32 zero-centred offset, bf16 round-to-nearest-even outputs);
-the returned values then lie exactly on those grids. ``rounded=False`` is the
+weight gradient, fp32 zero-centred offset, round-to-nearest-even activation
+outputs in the format ``fmt``: ``"bf16"``, the default, or ``"f16"``); the
+returned values then lie exactly on those grids. ``rounded=False`` is the
 unrounded mathematical function, used by finite-difference pins.
+
+The gated functions take ``gate``: ``"silu"`` (the default) or ``"sigmoid"``.
 
 ``eps`` is an fp32 argument of the library, so in rounded mode it is first
 rounded to fp32; in unrounded mode it is used as given.
@@ -38,7 +41,7 @@ import numpy as np
 from . import build as _build
 
 __all__ = [
-    "round_bf16", "num_threads",
+    "round_bf16", "round_f16", "num_threads",
     "rmsnorm_fwd", "rmsnorm_bwd", "residual_fwd", "residual_bwd",
     "gated_fwd", "gated_bwd", "weight_grad", "fused_add_fwd", "fused_add_bwd", "gated_hf_fwd",
     "gated_hf_apply",
@@ -60,12 +63,14 @@ def _load():
             lib.orc_num_threads.restype = _INT
             lib.orc_round_bf16.restype = ctypes.c_double
             lib.orc_round_bf16.argtypes = [ctypes.c_double]
+            lib.orc_round_f16.restype = ctypes.c_double
+            lib.orc_round_f16.argtypes = [ctypes.c_double]
             lib.orc_rmsnorm_fwd.argtypes = [_I64, _I64, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
             lib.orc_rmsnorm_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D, _D, _D]
-            lib.orc_gated_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
-            lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _D, _D, _D,
+            lib.orc_gated_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _INT, _D, _D]
+            lib.orc_gated_bwd.argtypes = [_I64, _I64, _D, _D, _D, _D, _D, _INT, _INT, _INT, _D, _D, _D,
                                           _D, _D, _D, _D, _D]
-            lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _D, _D]
+            lib.orc_weight_grad.argtypes = [_I64, _I64, _D, _D, _INT, _D, _D, _INT, _D, _D]
             lib.orc_gated_hf_fwd.argtypes = [_I64, _I64, _D, _D, _D, ctypes.c_double, _INT, _INT, _D, _D]
             lib.orc_gated_hf_fwd.restype = None
             lib.orc_gated_hf_apply.argtypes = [_I64, _I64, _D, _D, _D, _D, _INT, _INT, _D]
@@ -95,6 +100,23 @@ def _eps(eps: float, rounded: bool) -> float:
     return float(np.float32(eps)) if rounded else float(eps)
 
 
+_FMT = {"bf16": 1, "f16": 2}
+_GATE = {"silu": 0, "sigmoid": 1}
+
+
+def _rnd(rounded: bool, fmt: str) -> int:
+    """The C side's `rounded` argument: 0 (unrounded) or the output format code."""
+    if fmt not in _FMT:
+        raise ValueError(f"fmt must be one of {sorted(_FMT)}, got {fmt!r}")
+    return _FMT[fmt] if rounded else 0
+
+
+def _gate(gate: str) -> int:
+    if gate not in _GATE:
+        raise ValueError(f"gate must be one of {sorted(_GATE)}, got {gate!r}")
+    return _GATE[gate]
+
+
 def num_threads() -> int:
     """Threads the oracle's parallel loops use (1 if built without OpenMP)."""
     return int(_load().orc_num_threads())
@@ -107,7 +129,14 @@ def round_bf16(v) -> np.ndarray:
     return np.vectorize(lib.orc_round_bf16, otypes=[np.float64])(v) if v.size else v.copy()
 
 
-def rmsnorm_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+def round_f16(v) -> np.ndarray:
+    """Round float64 values to IEEE fp16 (nearest, ties to even) in one step; returns float64."""
+    lib = _load()
+    v = np.asarray(v, dtype=np.float64)
+    return np.vectorize(lib.orc_round_f16, otypes=[np.float64])(v) if v.size else v.copy()
+
+
+def rmsnorm_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True, fmt: str = "bf16"):
     """Plain / zero-centred forward. Returns ``(y [T,D], rstd [T])``."""
     x = _arr(x)
     T, D = x.shape
@@ -115,16 +144,16 @@ def rmsnorm_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bo
     y = np.empty((T, D))
     rstd = np.empty((T,))
     _load().orc_rmsnorm_fwd(T, D, _p(x), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
-                            int(rounded), _p(y), _p(rstd))
+                            _rnd(rounded, fmt), _p(y), _p(rstd))
     return y, rstd
 
 
 def rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma: bool = False, g_res=None,
-                rounded: bool = True, diagnostics: bool = False):
+                rounded: bool = True, diagnostics: bool = False, fmt: str = "bf16"):
     """Plain / zero-centred backward (``g_res`` adds the residual branch's gradient).
 
     ``rstd`` is the forward's saved inverse RMS. Returns ``(dx [T,D], dgamma [D])``,
-    plus, with ``diagnostics``, a dict with ``dx_pre`` (dx before its bf16
+    plus, with ``diagnostics``, a dict with ``dx_pre`` (dx before its final
     rounding), ``dx_scale`` (magnitude of dx's terms before cancellation) and
     ``dw_abs`` (sum of |terms| of each weight-gradient column).
     """
@@ -139,12 +168,12 @@ def rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma: bool = False, g_res=None,
     diag = {k: np.empty(s) for k, s in (("dx_pre", (T, D)), ("dx_scale", (T, D)), ("dw_abs", (D,)))} \
         if diagnostics else {}
     _load().orc_rmsnorm_bwd(T, D, _p(g), _p(x), _p(w), _p(rstd), _p(gr),
-                            int(zero_centered_gamma), int(rounded), _p(dx), _p(dw),
+                            int(zero_centered_gamma), _rnd(rounded, fmt), _p(dx), _p(dw),
                             _p(diag.get("dx_pre")), _p(diag.get("dx_scale")), _p(diag.get("dw_abs")))
     return (dx, dw, diag) if diagnostics else (dx, dw)
 
 
-def residual_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+def residual_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True, fmt: str = "bf16"):
     """``rmsnorm_residual`` forward: the normalised output plus a copy of the input.
 
     The copy is the input itself, unchanged ([Residual], Summary: the op returns
@@ -152,20 +181,21 @@ def residual_fwd(x, w, eps: float, zero_centered_gamma: bool = False, rounded: b
     RMSNorm(x + residual)). Returns ``(y, rstd, x_copy)``.
     """
     x = _arr(x)
-    y, rstd = rmsnorm_fwd(x, w, eps, zero_centered_gamma, rounded)
+    y, rstd = rmsnorm_fwd(x, w, eps, zero_centered_gamma, rounded, fmt)
     return y, rstd, x.copy()
 
 
 def residual_bwd(g, x, w, rstd, g_res, zero_centered_gamma: bool = False, rounded: bool = True,
-                 diagnostics: bool = False):
+                 diagnostics: bool = False, fmt: str = "bf16"):
     """``rmsnorm_residual`` backward: ``dx`` gains the copy branch's gradient ``g_res``
     before its single rounding ([Residual], reviewer's "for dx": ``+ d_residual``)."""
     return rmsnorm_bwd(g, x, w, rstd, zero_centered_gamma, g_res=g_res, rounded=rounded,
-                       diagnostics=diagnostics)
+                       diagnostics=diagnostics, fmt=fmt)
 
 
-def gated_fwd(x, z, w, eps: float, zero_centered_gamma: bool = True, rounded: bool = True):
-    """Gated forward ``y = ((x r) w_eff) silu(z)``. Returns ``(y, rstd)``."""
+def gated_fwd(x, z, w, eps: float, zero_centered_gamma: bool = True, rounded: bool = True,
+              gate: str = "silu", fmt: str = "bf16"):
+    """Gated forward ``y = ((x r) w_eff) q(z)``, q = silu or sigmoid. Returns ``(y, rstd)``."""
     x = _arr(x)
     T, D = x.shape
     z = _arr(z, (T, D))
@@ -173,15 +203,15 @@ def gated_fwd(x, z, w, eps: float, zero_centered_gamma: bool = True, rounded: bo
     y = np.empty((T, D))
     rstd = np.empty((T,))
     _load().orc_gated_fwd(T, D, _p(x), _p(z), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
-                          int(rounded), _p(y), _p(rstd))
+                          _gate(gate), _rnd(rounded, fmt), _p(y), _p(rstd))
     return y, rstd
 
 
 def gated_bwd(g, x, z, w, rstd, zero_centered_gamma: bool = True, rounded: bool = True,
-              diagnostics: bool = False):
+              diagnostics: bool = False, gate: str = "silu", fmt: str = "bf16"):
     """Gated backward. Returns ``(dx [T,D], dz [T,D], dw [D])``, plus with
     ``diagnostics`` a dict as in ``rmsnorm_bwd`` with ``dz_pre`` and ``dz_scale``
-    (|g u| sig (1 + |z| (1 - sig))) added."""
+    (|g u| times q' with its cancelling term in absolute value) added."""
     x = _arr(x)
     T, D = x.shape
     g = _arr(g, (T, D))
@@ -195,13 +225,13 @@ def gated_bwd(g, x, z, w, rstd, zero_centered_gamma: bool = True, rounded: bool 
              ("dw_abs", (D,)))
     diag = {k: np.empty(s) for k, s in names} if diagnostics else {}
     _load().orc_gated_bwd(T, D, _p(g), _p(x), _p(z), _p(w), _p(rstd), int(zero_centered_gamma),
-                          int(rounded), _p(dx), _p(dz), _p(dw),
+                          _gate(gate), _rnd(rounded, fmt), _p(dx), _p(dz), _p(dw),
                           *[_p(diag.get(k)) for k, _ in names])
     return (dx, dz, dw, diag) if diagnostics else (dx, dz, dw)
 
 
-def weight_grad(g, x, rstd, z=None, rounded: bool = True, with_abs: bool = False):
-    """Weight gradient alone, ``sum_t g_tj [silu(z_tj)] x_tj r_t`` per column.
+def weight_grad(g, x, rstd, z=None, rounded: bool = True, with_abs: bool = False, gate: str = "silu"):
+    """Weight gradient alone, ``sum_t g_tj [q(z_tj)] x_tj r_t`` per column.
 
     Columns are independent, so this may be called on any subset of columns
     (with all T rows) to check sampled columns of a large problem; pass the
@@ -215,13 +245,14 @@ def weight_grad(g, x, rstd, z=None, rounded: bool = True, with_abs: bool = False
     zz = None if z is None else _arr(z, (T, D))
     dw = np.empty((D,))
     dwa = np.empty((D,)) if with_abs else None
-    _load().orc_weight_grad(T, D, _p(g), _p(zz), _p(x), _p(rstd), int(rounded), _p(dw), _p(dwa))
+    _load().orc_weight_grad(T, D, _p(g), _p(zz), _gate(gate), _p(x), _p(rstd), int(rounded), _p(dw), _p(dwa))
     return (dw, dwa) if with_abs else dw
 
 
-def fused_add_fwd(x, res, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True):
+def fused_add_fwd(x, res, w, eps: float, zero_centered_gamma: bool = False, rounded: bool = True,
+                  fmt: str = "bf16"):
     """Fused add + norm forward on h = x + res (fp32 sum). Returns ``(y, rstd, res_out)``
-    with ``res_out`` = bf16(h) (rounded mode) or h (unrounded)."""
+    with ``res_out`` = h rounded to ``fmt`` (rounded mode) or h (unrounded)."""
     x = _arr(x)
     T, D = x.shape
     res = _arr(res, (T, D))
@@ -230,12 +261,12 @@ def fused_add_fwd(x, res, w, eps: float, zero_centered_gamma: bool = False, roun
     rstd = np.empty((T,))
     ro = np.empty((T, D))
     _load().orc_fused_add_fwd(T, D, _p(x), _p(res), _p(w), _eps(eps, rounded), int(zero_centered_gamma),
-                              int(rounded), _p(y), _p(rstd), _p(ro))
+                              _rnd(rounded, fmt), _p(y), _p(rstd), _p(ro))
     return y, rstd, ro
 
 
 def fused_add_bwd(g, x, res, w, rstd, g_res=None, zero_centered_gamma: bool = False, rounded: bool = True,
-                  diagnostics: bool = False):
+                  diagnostics: bool = False, fmt: str = "bf16"):
     """Fused add + norm backward. Returns ``(dh [T,D], dgamma [D])`` (+ diagnostics as in
     ``rmsnorm_bwd``); ``dh`` is the gradient of both x and res."""
     x = _arr(x)
@@ -251,7 +282,7 @@ def fused_add_bwd(g, x, res, w, rstd, g_res=None, zero_centered_gamma: bool = Fa
     diag = {k: np.empty(s) for k, s in (("dx_pre", (T, D)), ("dx_scale", (T, D)), ("dw_abs", (D,)))} \
         if diagnostics else {}
     _load().orc_fused_add_bwd(T, D, _p(g), _p(x), _p(res), _p(w), _p(rstd), _p(gr), int(zero_centered_gamma),
-                              int(rounded), _p(dh), _p(dw), _p(hs), _p(diag.get("dx_pre")),
+                              _rnd(rounded, fmt), _p(dh), _p(dw), _p(hs), _p(diag.get("dx_pre")),
                               _p(diag.get("dx_scale")), _p(diag.get("dw_abs")))
     return (dh, dw, diag) if diagnostics else (dh, dw)
 

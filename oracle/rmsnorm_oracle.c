@@ -13,13 +13,15 @@
  *   [Residual]  RL-Kernel pull request 414, "[DSv4][P1-5] rmsnorm_residual"
  *
  * Everything is evaluated in IEEE double. Rounding happens only at the points
- * the method states, and only when `rounded` is non-zero:
+ * the method states, and only when `rounded` is non-zero. Its value names the
+ * activation format: 1 = bf16, 2 = fp16 ([ZC-norm]: the op contract carries
+ * tolerances for both; the arithmetic between load and store is the same).
  *   - the saved inverse RMS is an fp32 value                  ([Residual], Implementation)
  *   - the zero-centred offset is an fp32 add after the fp32 cast
  *                                     ([Megatron], What does this PR do, item 1;
  *                                      [ZC-norm], the GemmaRMSNorm forward_native note)
- *   - activations and activation gradients are bf16, rounded to nearest even
- *                                                             ([Residual], Implementation)
+ *   - activations and activation gradients are bf16 (or fp16), rounded to
+ *     nearest even                                            ([Residual], Implementation)
  *   - the weight gradient is an fp32 value                    ([Residual], Implementation)
  * With `rounded == 0` nothing is rounded: that mode is the plain mathematical
  * function, used by the finite-difference checks.
@@ -62,10 +64,33 @@ double orc_round_bf16(double v) {
     return signbit(v) ? -r : r;
 }
 
+/* Round a double to the nearest IEEE binary16 value (11 significant bits,
+ * normal exponents -14..15, subnormal quantum 2^-24), ties to even, in ONE
+ * rounding step from the double; overflow (a result of 2^16 or beyond) is
+ * infinite. Returns the rounded value as a double. */
+double orc_round_f16(double v) {
+    if (isnan(v)) return v;
+    if (isinf(v)) return v;
+    double a = fabs(v);
+    if (a == 0.0) return v;
+    int E;
+    (void)frexp(a, &E);
+    int e = E - 1;                     /* a in [2^e, 2^(e+1)) */
+    int q = (e < -14) ? -24 : e - 10;  /* quantum exponent */
+    double r = ldexp(nearbyint(ldexp(a, -q)), q);
+    if (r >= ldexp(1.0, 16)) r = INFINITY;
+    return signbit(v) ? -r : r;
+}
+
 /* Round a double to fp32 (C conversion, round to nearest even). */
 static double fl32(double v) { return (double)(float)v; }
 
-static double maybe_bf16(double v, int rounded) { return rounded ? orc_round_bf16(v) : v; }
+/* An activation output in the format `rounded` names (0: unrounded). */
+static double maybe_act(double v, int rounded) {
+    if (rounded == 1) return orc_round_bf16(v);
+    if (rounded == 2) return orc_round_f16(v);
+    return v;
+}
 static double maybe_fl32(double v, int rounded) { return rounded ? fl32(v) : v; }
 
 /* Effective weight: w, or w + 1 applied in fp32 after the fp32 cast when the
@@ -89,6 +114,24 @@ static double row_inv_rms(const double* x, int64_t D, double eps) {
 static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }
 static double silu(double z) { return z * sigmoid(z); }
 
+/* The gated norm's gate q(z): silu (gate 0, the default) or sigmoid (gate 1)
+ * ([ZC-norm]: the activation is read from the model config, silu by default,
+ * sigmoid also allowed), and its derivative q'(z):
+ *   silu:    q' = sigmoid(z) (1 + z (1 - sigmoid(z)))
+ *   sigmoid: q' = sigmoid(z) (1 - sigmoid(z)) = sigmoid(z) sigmoid(-z)
+ * gate_dq_scale is q' with the cancelling term taken in absolute value: the
+ * magnitude of the terms q' is made of (for the tolerance of a finite-precision
+ * evaluation of q'). */
+static double gate_q(double z, int gate) { return gate ? sigmoid(z) : silu(z); }
+static double gate_dq(double z, int gate) {
+    double sg = sigmoid(z);
+    return gate ? sg * sigmoid(-z) : sg * (1.0 + z * (1.0 - sg));
+}
+static double gate_dq_scale(double z, int gate) {
+    double sg = sigmoid(z);
+    return gate ? sg * sigmoid(-z) : sg * (1.0 + fabs(z) * (1.0 - sg));
+}
+
 /* ------------------------------------------------------------------------ */
 /* Plain / zero-centred forward:  y = (x * r) * w_eff,  rstd = r              */
 /* ([Megatron], item 1; [Residual], reviewer's "Forward" summary)            */
@@ -101,27 +144,27 @@ void orc_rmsnorm_fwd(int64_t T, int64_t D, const double* x, const double* w, dou
         double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);
         rstd[t] = r;
         for (int64_t j = 0; j < D; ++j)
-            y[t * D + j] = maybe_bf16(xr[j] * r * w_eff(w[j], zero_centered, rounded), rounded);
+            y[t * D + j] = maybe_act(xr[j] * r * w_eff(w[j], zero_centered, rounded), rounded);
     }
 }
 
 /* ------------------------------------------------------------------------ */
 /* Weight gradient: dgamma_j = sum_t g_tj * x_tj * r_t  (ascending t)         */
 /* ([Megatron], item 2, g_w unchanged; [Residual], reviewer's "for dgamma")  */
-/* Gated variant (z != NULL): g is replaced by g * silu(z), the gradient that */
-/* reaches the normalised-and-scaled value.                                   */
+/* Gated variant (z != NULL): g is replaced by g * q(z) (gate as in gate_q),  */
+/* the gradient that reaches the normalised-and-scaled value.                 */
 /* Columns are independent: any column subset may be passed with all T rows.  */
 /* dw_abs (may be NULL) receives sum_t |term|, the scale of the rounding     */
 /* error any finite-precision evaluation of the sum can make.                */
 /* ------------------------------------------------------------------------ */
-void orc_weight_grad(int64_t T, int64_t D, const double* g, const double* z,
+void orc_weight_grad(int64_t T, int64_t D, const double* g, const double* z, int gate,
                      const double* x, const double* r, int rounded, double* dw, double* dw_abs) {
 #pragma omp parallel for schedule(static)
     for (int64_t j = 0; j < D; ++j) {
         double acc = 0.0, mag = 0.0;
         for (int64_t t = 0; t < T; ++t) {
             double gt = g[t * D + j];
-            if (z) gt *= silu(z[t * D + j]);
+            if (z) gt *= gate_q(z[t * D + j], gate);
             double term = gt * x[t * D + j] * r[t];
             acc += term;
             mag += fabs(term);
@@ -163,21 +206,21 @@ void orc_rmsnorm_bwd(int64_t T, int64_t D, const double* g, const double* x, con
             double v = a - b;
             double mag = fabs(a) + (r * r * r * fabs(xr[k]) / (double)D) * s_abs;
             if (g_res) { v += g_res[t * D + k]; mag += fabs(g_res[t * D + k]); }
-            dx[t * D + k] = maybe_bf16(v, rounded);
+            dx[t * D + k] = maybe_act(v, rounded);
             if (dx_pre) dx_pre[t * D + k] = v;
             if (dx_scale) dx_scale[t * D + k] = mag;
         }
     }
-    orc_weight_grad(T, D, g, NULL, x, rstd, rounded, dw, dw_abs);
+    orc_weight_grad(T, D, g, NULL, 0, x, rstd, rounded, dw, dw_abs);
 }
 
 /* ------------------------------------------------------------------------ */
 /* Gated forward (Qwen3-Next, vLLM convention: weight multiply in fp32):      */
-/*   u = (x * r) * w_eff,  y = u * silu(z)                                    */
+/*   u = (x * r) * w_eff,  y = u * q(z),  q = silu (gate 0) or sigmoid (1)    */
 /* ([ZC-norm], the two gated-norm conventions: Qwen3NextRMSNormGatedOp)      */
 /* ------------------------------------------------------------------------ */
 void orc_gated_fwd(int64_t T, int64_t D, const double* x, const double* z, const double* w,
-                   double eps, int zero_centered, int rounded, double* y, double* rstd) {
+                   double eps, int zero_centered, int gate, int rounded, double* y, double* rstd) {
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         const double* xr = x + t * D;
@@ -185,24 +228,24 @@ void orc_gated_fwd(int64_t T, int64_t D, const double* x, const double* z, const
         rstd[t] = r;
         for (int64_t j = 0; j < D; ++j) {
             double u = xr[j] * r * w_eff(w[j], zero_centered, rounded);
-            y[t * D + j] = maybe_bf16(u * silu(z[t * D + j]), rounded);
+            y[t * D + j] = maybe_act(u * gate_q(z[t * D + j], gate), rounded);
         }
     }
 }
 
 /* ------------------------------------------------------------------------ */
-/* Gated backward. With q = silu(z) and u = x r w_eff (so y = u q):           */
+/* Gated backward. With q = q(z) and u = x r w_eff (so y = u q):             */
 /*   dL/du = g q, which enters the plain backward in place of g:              */
 /*     s    = sum_i (g_i q_i) x_i w_eff_i                                     */
 /*     dx_k = (g_k q_k) w_eff_k r - (r^3 x_k / D) * s                         */
-/*   dz_k = g_k u_k silu'(z_k),  silu'(z) = sig(z) (1 + z (1 - sig(z)))       */
+/*   dz_k = g_k u_k q'(z_k)                                                   */
 /*   dw_j = sum_t g_tj q_tj x_tj r_t                                          */
 /* ------------------------------------------------------------------------ */
 void orc_gated_bwd(int64_t T, int64_t D, const double* g, const double* x, const double* z,
-                   const double* w, const double* rstd, int zero_centered, int rounded,
+                   const double* w, const double* rstd, int zero_centered, int gate, int rounded,
                    double* dx, double* dz, double* dw,
                    double* dx_pre, double* dx_scale, double* dz_pre, double* dz_scale, double* dw_abs) {
-    /* Diagnostics as in orc_rmsnorm_bwd; dz_scale = |g u| sig (1 + |z| (1 - sig)). */
+    /* Diagnostics as in orc_rmsnorm_bwd; dz_scale = |g u| gate_dq_scale(z). */
 #pragma omp parallel for schedule(static)
     for (int64_t t = 0; t < T; ++t) {
         const double* gr = g + t * D;
@@ -211,36 +254,35 @@ void orc_gated_bwd(int64_t T, int64_t D, const double* g, const double* x, const
         double r = rstd[t];
         double s = 0.0, s_abs = 0.0;
         for (int64_t i = 0; i < D; ++i) {
-            double term = gr[i] * silu(zr[i]) * xr[i] * w_eff(w[i], zero_centered, rounded);
+            double term = gr[i] * gate_q(zr[i], gate) * xr[i] * w_eff(w[i], zero_centered, rounded);
             s += term;
             s_abs += fabs(term);
         }
         for (int64_t k = 0; k < D; ++k) {
             double we = w_eff(w[k], zero_centered, rounded);
-            double a = gr[k] * silu(zr[k]) * we * r;
+            double a = gr[k] * gate_q(zr[k], gate) * we * r;
             double v = a - (r * r * r * xr[k] / (double)D) * s;
-            dx[t * D + k] = maybe_bf16(v, rounded);
+            dx[t * D + k] = maybe_act(v, rounded);
             if (dx_pre) dx_pre[t * D + k] = v;
             if (dx_scale) dx_scale[t * D + k] = fabs(a) + (r * r * r * fabs(xr[k]) / (double)D) * s_abs;
-            double sg = sigmoid(zr[k]);
             double u = xr[k] * r * we;
-            double d = gr[k] * u * (sg * (1.0 + zr[k] * (1.0 - sg)));
-            dz[t * D + k] = maybe_bf16(d, rounded);
+            double d = gr[k] * u * gate_dq(zr[k], gate);
+            dz[t * D + k] = maybe_act(d, rounded);
             if (dz_pre) dz_pre[t * D + k] = d;
-            if (dz_scale) dz_scale[t * D + k] = fabs(gr[k] * u) * (sg * (1.0 + fabs(zr[k]) * (1.0 - sg)));
+            if (dz_scale) dz_scale[t * D + k] = fabs(gr[k] * u) * gate_dq_scale(zr[k], gate);
         }
     }
-    orc_weight_grad(T, D, g, z, x, rstd, rounded, dw, dw_abs);
+    orc_weight_grad(T, D, g, z, gate, x, rstd, rounded, dw, dw_abs);
 }
 
 /* ------------------------------------------------------------------------ */
 /* Fused add + RMSNorm (vLLM fused_add_rms_norm, the decoder-norm path of     */
 /* [ZC-norm], "Only layer 0's input norm takes the no-residual path"): the   */
 /* norm is applied to the fp32 sum h = x + res, which is also returned       */
-/* rounded to bf16 as the new residual stream.                               */
-/*   h = fl32(x + res);  res_out = bf16(h);  rstd, y as the plain forward on h */
+/* rounded to the activation format as the new residual stream.             */
+/*   h = fl32(x + res);  res_out = act(h);  rstd, y as the plain forward on h  */
 /* Reading (the pages give no rounding order): the sum is one fp32 add; the  */
-/* normalisation uses that fp32 h, not its bf16 rounding.                    */
+/* normalisation uses that fp32 h, not its rounding to the activation format. */
 /* ------------------------------------------------------------------------ */
 void orc_fused_add_fwd(int64_t T, int64_t D, const double* x, const double* res, const double* w,
                        double eps, int zero_centered, int rounded,
@@ -252,8 +294,8 @@ void orc_fused_add_fwd(int64_t T, int64_t D, const double* x, const double* res,
         double r = maybe_fl32(row_inv_rms(h, D, eps), rounded);
         rstd[t] = r;
         for (int64_t j = 0; j < D; ++j) {
-            y[t * D + j] = maybe_bf16(h[j] * r * w_eff(w[j], zero_centered, rounded), rounded);
-            h[j] = maybe_bf16(h[j], rounded);
+            y[t * D + j] = maybe_act(h[j] * r * w_eff(w[j], zero_centered, rounded), rounded);
+            h[j] = maybe_act(h[j], rounded);
         }
     }
 }
@@ -292,10 +334,10 @@ void orc_gated_hf_apply(int64_t T, int64_t D, const double* x, const double* z, 
     for (int64_t t = 0; t < T; ++t) {
         const double r = rstd[t];
         for (int64_t j = 0; j < D; ++j) {
-            double n = maybe_bf16(maybe_fl32(x[t * D + j] * r, rounded), rounded);
-            double wb = maybe_bf16(w_eff(w[j], zero_centered, rounded), rounded);
-            double tt = maybe_bf16(maybe_fl32(wb * n, rounded), rounded);
-            y[t * D + j] = maybe_bf16(tt * silu(z[t * D + j]), rounded);
+            double n = maybe_act(maybe_fl32(x[t * D + j] * r, rounded), rounded);
+            double wb = maybe_act(w_eff(w[j], zero_centered, rounded), rounded);
+            double tt = maybe_act(maybe_fl32(wb * n, rounded), rounded);
+            y[t * D + j] = maybe_act(tt * silu(z[t * D + j]), rounded);
         }
     }
 }

@@ -13,17 +13,28 @@ import torch
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
-    """Exact conversion of a bf16/fp32 tensor (any device) to a float64 numpy array."""
+    """Exact conversion of a bf16/fp16/fp32 tensor (any device) to a float64 numpy array."""
     return t.detach().to("cpu", torch.float32).numpy().astype(np.float64)
 
 
 def bf16_ulp(v: np.ndarray) -> np.ndarray:
     """Spacing of bf16 numbers at |v| (the gap to the next larger magnitude)."""
+    return act_ulp(v, "bf16")
+
+
+# (fraction bits, smallest normal exponent) of each activation format
+_FORMATS = {"bf16": (7, -126), "f16": (10, -14)}
+
+
+def act_ulp(v: np.ndarray, fmt: str = "bf16") -> np.ndarray:
+    """Spacing of ``fmt`` numbers at |v| (the gap to the next larger magnitude;
+    the subnormal spacing below the normal range)."""
+    mant, emin = _FORMATS[fmt]
     a = np.abs(np.asarray(v, dtype=np.float64))
     e = np.floor(np.log2(np.where(a > 0, a, 1.0)))
-    e = np.where(a > 0, e, -126.0)
-    e = np.maximum(e, -126.0)
-    return np.exp2(e - 7.0)
+    e = np.where(a > 0, e, float(emin))
+    e = np.maximum(e, float(emin))
+    return np.exp2(e - float(mant))
 
 
 # --------------------------------------------------------------------------
@@ -41,10 +52,30 @@ def _bf16_table():
     return _BF16_POS
 
 
+_F16_POS = None
+
+
+def _f16_table():
+    global _F16_POS
+    if _F16_POS is None:
+        bits = torch.arange(0, 0x7C00, dtype=torch.int32).to(torch.int16)
+        vals = bits.view(torch.float16).to(torch.float64).tolist()
+        _F16_POS = [Fraction(v) for v in vals]  # ascending, 0 .. 65504
+    return _F16_POS
+
+
 def bf16_round_bruteforce(v) -> float:
     """Nearest bf16 value to the exact rational ``v`` (ties to the even bit pattern)."""
+    return _round_bruteforce(v, _bf16_table())
+
+
+def f16_round_bruteforce(v) -> float:
+    """Nearest IEEE fp16 value to the exact rational ``v`` (ties to the even bit pattern)."""
+    return _round_bruteforce(v, _f16_table())
+
+
+def _round_bruteforce(v, tab) -> float:
     v = Fraction(v)
-    tab = _bf16_table()
     a = abs(v)
     top = tab[-1]
     half_gap_top = (top - tab[-2]) / 2
@@ -91,39 +122,39 @@ def fd_grad(loss, arr: np.ndarray, h: float = 1e-5) -> np.ndarray:
 U32 = 2.0 ** -24
 
 
-def check_bf16_within_1ulp(got: np.ndarray, ref_rounded: np.ndarray):
-    """Spec bar for bf16 outputs: |got - RN(ref)| <= 1 bf16 ulp of RN(ref).
-    Returns the boolean pass mask."""
+def check_bf16_within_1ulp(got: np.ndarray, ref_rounded: np.ndarray, fmt: str = "bf16"):
+    """Spec bar for 16-bit outputs: |got - RN(ref)| <= 1 ulp of RN(ref) in
+    the output format ``fmt`` (bf16, or fp16). Returns the boolean pass mask."""
     got = np.asarray(got, np.float64)
     ref = np.asarray(ref_rounded, np.float64)
     same_special = (np.isnan(got) & np.isnan(ref)) | (np.isinf(got) & (got == ref))
-    return same_special | (np.abs(got - ref) <= bf16_ulp(ref))
+    return same_special | (np.abs(got - ref) <= act_ulp(ref, fmt))
 
 
-def _ulp_of_max(a, b):
-    return bf16_ulp(np.maximum(np.abs(a), np.abs(b)))
+def _ulp_of_max(a, b, fmt="bf16"):
+    return act_ulp(np.maximum(np.abs(a), np.abs(b)), fmt)
 
 
-def bf16_parity_mask(got, ref_rounded, pre=None, scale=None, K: float = 96.0):
-    """Parity of a bf16 output with the oracle.
+def bf16_parity_mask(got, ref_rounded, pre=None, scale=None, K: float = 96.0, fmt: str = "bf16"):
+    """Parity of a 16-bit output (format ``fmt``, bf16 by default) with the oracle.
 
-    Clause 1 (the bar): |got - RN(ref)| <= 1 bf16 ulp of RN(ref).
+    Clause 1 (the bar): |got - RN(ref)| <= 1 ulp of RN(ref).
     Clause 2 (only with ``pre``/``scale``, for outputs whose terms cancel):
     |got - ref| <= 1/2 ulp + K * 2^-24 * scale, where ``ref`` is the exact
     pre-rounding value and ``scale`` the magnitude of its terms: the error an
     fp32 evaluation with at most K separately rounded steps can make, plus the
-    final bf16 rounding. Returns (mask, n_clause2).
+    final rounding to the output format. Returns (mask, n_clause2).
     """
     got = np.asarray(got, np.float64)
-    m1 = check_bf16_within_1ulp(got, ref_rounded)
+    m1 = check_bf16_within_1ulp(got, ref_rounded, fmt)
     if pre is None:
         return m1, 0
-    m2 = np.abs(got - pre) <= 0.5 * _ulp_of_max(got, pre) + K * U32 * scale
+    m2 = np.abs(got - pre) <= 0.5 * _ulp_of_max(got, pre, fmt) + K * U32 * scale
     return m1 | m2, int(np.count_nonzero(m2 & ~m1))
 
 
-def assert_bf16_parity(name, got, ref_rounded, pre=None, scale=None, K: float = 96.0):
-    mask, n2 = bf16_parity_mask(got, ref_rounded, pre, scale, K)
+def assert_bf16_parity(name, got, ref_rounded, pre=None, scale=None, K: float = 96.0, fmt: str = "bf16"):
+    mask, n2 = bf16_parity_mask(got, ref_rounded, pre, scale, K, fmt)
     bad = np.argwhere(~mask)
     if bad.size:
         i = tuple(bad[0])
