@@ -27,9 +27,10 @@
  * from run to run and across GPUs with different SM counts.
  *
  * Common conventions for every entry point:
- *   - Activations (x, z, g, g_res, y, dx, dz, x_copy) are bf16, row-major [T][D]
- *     with a row stride `ld*` in ELEMENTS (ld >= D). They are passed as raw bf16
- *     bit patterns (rmsn_bf16). w / dgamma are fp32 [D]; rstd is fp32 [T].
+ *   - Activations (x, z, g, g_res, y, dx, dz, x_copy) are bf16 (fp16 as an
+ *     option of the *_ex calls), row-major [T][D] with a row stride `ld*` in
+ *     ELEMENTS (ld >= D). They are passed as raw 16-bit patterns (rmsn_bf16,
+ *     rmsn_act16). w / dgamma are fp32 [D]; rstd is fp32 [T].
  *   - All pointers are DEVICE pointers, 16-byte aligned; every ld* is a multiple
  *     of 8 (so each row starts on a 16-byte boundary). D is a multiple of 8 with
  *     8 <= D <= 16384. eps is finite and >= 0. 0 <= T < 2^31; T == 0 returns
@@ -60,6 +61,7 @@ extern "C" {
 #endif
 
 typedef uint16_t rmsn_bf16;               /* raw bf16 bit pattern                      */
+typedef uint16_t rmsn_act16;              /* raw 16-bit activation, bf16 or fp16 by `dtype` */
 typedef struct CUstream_st* rmsn_stream;  /* identical to cudaStream_t; NULL = default */
 
 enum rmsn_status {
@@ -69,6 +71,18 @@ enum rmsn_status {
     RMSN_EUNSUPPORTED = -3,  /* D outside [8, 16384] or not a multiple of 8             */
     RMSN_ECUDA = -4,         /* a CUDA runtime or driver call failed                    */
     RMSN_EWORKSPACE = -5     /* workspace missing or smaller than the query's answer    */
+};
+
+/* Activation storage formats of the *_ex entry points. */
+enum rmsn_dtype {
+    RMSN_DTYPE_BF16 = 0,     /* bfloat16 (what every entry point without _ex takes)     */
+    RMSN_DTYPE_F16 = 1       /* IEEE binary16                                           */
+};
+
+/* Gate activation of the gated norm (*_ex entry points). */
+enum rmsn_gate {
+    RMSN_GATE_SILU = 0,      /* q(z) = z * sigmoid(z) (what rmsnorm_gated_fwd/bwd use)  */
+    RMSN_GATE_SIGMOID = 1    /* q(z) = sigmoid(z)                                       */
 };
 
 /* Human-readable name of a status code (static string). */
@@ -186,6 +200,80 @@ int rmsnorm_gated_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16
                                 rmsn_bf16* y, int64_t ldy,
                                 void* ws, size_t ws_bytes,
                                 int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
+
+/* ------------------------------------------------------------------------
+ * Activation dtype and gate options ([ZC-norm]: the gated norm's activation
+ * is configurable, silu by default with sigmoid allowed; the op contract's
+ * tolerances cover fp16 activations beside bf16).
+ *
+ * Each *_ex entry point is the entry point of the same name without the
+ * suffix, with two changes:
+ *   - `dtype` (enum rmsn_dtype) names the storage format of EVERY activation
+ *     argument (inputs and outputs alike): RMSN_DTYPE_BF16 gives exactly the
+ *     unsuffixed call's results; with RMSN_DTYPE_F16 every activation is an
+ *     IEEE binary16 bit pattern, widened exactly to fp32 on load, and every
+ *     activation output is rounded from the same fp32 value to the nearest
+ *     fp16 (ties to even; subnormals kept; overflow gives infinity). w, rstd
+ *     and dgamma stay fp32, and the fp32 arithmetic, its reduction trees and
+ *     the batch-invariance and determinism guarantees are unchanged.
+ *   - the gated calls take `gate` (enum rmsn_gate). With RMSN_GATE_SIGMOID:
+ *       y  = round( ((x * r) * w_eff) * sigmoid(z) ),
+ *       backward: dx as rmsnorm_bwd with g * sigmoid(z) in place of g;
+ *       dz = round( g * u * sigmoid(z) * sigmoid(-z) ),  u = (x * r) * w_eff;
+ *       dw_j = sum_t g sigmoid(z) x r.
+ * An unknown dtype or gate is RMSN_EINVAL. Alignment, ownership, workspace
+ * and error behaviour as the unsuffixed call.
+ * ------------------------------------------------------------------------ */
+int rmsnorm_fwd_ex(const rmsn_act16* x, int64_t ldx, const float* w,
+                   rmsn_act16* y, int64_t ldy, float* rstd,
+                   int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                   int dtype, rmsn_stream stream);
+
+int rmsnorm_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                   const float* w, const float* rstd,
+                   rmsn_act16* dx, int64_t lddx, float* dgamma,
+                   void* ws, size_t ws_bytes,
+                   int64_t T, int64_t D, int zero_centered_gamma, int dtype, rmsn_stream stream);
+
+int rmsnorm_residual_fwd_ex(const rmsn_act16* x, int64_t ldx, const float* w,
+                            rmsn_act16* y, int64_t ldy, float* rstd,
+                            rmsn_act16* x_copy, int64_t ldxc,
+                            int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                            int dtype, rmsn_stream stream);
+
+int rmsnorm_residual_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                            const float* w, const float* rstd,
+                            const rmsn_act16* g_res, int64_t ldgr,
+                            rmsn_act16* dx, int64_t lddx, float* dgamma,
+                            void* ws, size_t ws_bytes,
+                            int64_t T, int64_t D, int zero_centered_gamma, int dtype,
+                            rmsn_stream stream);
+
+int rmsnorm_gated_fwd_ex(const rmsn_act16* x, int64_t ldx, const rmsn_act16* z, int64_t ldz,
+                         const float* w, rmsn_act16* y, int64_t ldy, float* rstd,
+                         int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                         int gate, int dtype, rmsn_stream stream);
+
+int rmsnorm_gated_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                         const rmsn_act16* z, int64_t ldz, const float* w, const float* rstd,
+                         rmsn_act16* dx, int64_t lddx, rmsn_act16* dz, int64_t lddz, float* dw,
+                         void* ws, size_t ws_bytes,
+                         int64_t T, int64_t D, int zero_centered_gamma, int gate, int dtype,
+                         rmsn_stream stream);
+
+int rmsnorm_fused_add_fwd_ex(const rmsn_act16* x, int64_t ldx, const rmsn_act16* res, int64_t ldres,
+                             const float* w, rmsn_act16* y, int64_t ldy, float* rstd,
+                             rmsn_act16* res_out, int64_t ldro,
+                             int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                             int dtype, rmsn_stream stream);
+
+int rmsnorm_fused_add_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                             const rmsn_act16* res, int64_t ldres, const float* w, const float* rstd,
+                             const rmsn_act16* g_res, int64_t ldgr,
+                             rmsn_act16* dh, int64_t lddh, float* dgamma,
+                             void* ws, size_t ws_bytes,
+                             int64_t T, int64_t D, int zero_centered_gamma, int dtype,
+                             rmsn_stream stream);
 
 /* Weight-gradient pass 2 on its own: sums the per-chunk partials that a backward
  * call with a NULL dgamma/dw left in ws (same T, D and workspace), in the fixed

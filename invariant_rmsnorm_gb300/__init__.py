@@ -8,8 +8,9 @@ name in ``_build/librmsnorm_gb300.so``. All arithmetic runs in the library's
 sm_103a kernels. If the library has not been built, ``load()`` raises; there is
 no other implementation to fall back to.
 
-Activations are bf16 ``[T, D]`` with unit column stride (any row stride that
-is a multiple of 8 elements); weights and weight gradients fp32 ``[D]``;
+Activations are bf16 ``[T, D]`` (bf16 or fp16 for the ``*_ex`` calls, which take
+the format from ``x``) with unit column stride (any row stride that is a
+multiple of 8 elements); weights and weight gradients fp32 ``[D]``;
 inverse RMS fp32 ``[T]``. Work is enqueued on ``stream`` (default: the current
 torch stream of the tensors' device).
 """
@@ -31,6 +32,9 @@ __all__ = [
     "rmsnorm_bwd_workspace_bytes", "rmsnorm_status_string", "rmsnorm_device_error",
     "rmsnorm_bwd_noalloc", "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_bwd_recompute",
     "rmsnorm_gated_bwd_recompute", "rmsnorm_gated_hf_fwd", "EXPORTED_SYMBOLS",
+    "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
+    "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
+    "DTYPE_CODES", "GATE_CODES",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -39,7 +43,13 @@ EXPORTED_SYMBOLS = (
     "rmsnorm_dgamma_reduce", "rmsnorm_device_error", "rmsnorm_bwd_noalloc",
     "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_bwd_recompute", "rmsnorm_gated_bwd_recompute",
     "rmsnorm_gated_hf_fwd",
+    "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
+    "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
 )
+
+# enum rmsn_dtype / enum rmsn_gate of include/rmsnorm.h
+DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1}
+GATE_CODES = {"silu": 0, "sigmoid": 1}
 
 _P = ctypes.c_void_p
 _I64 = ctypes.c_int64
@@ -70,6 +80,13 @@ _SIGS = {
     "rmsnorm_gated_bwd_recompute": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64,
                                            _P, _SZ, _I64, _I64, _INT, _P]),
 }
+# Each *_ex call: the unsuffixed signature with `int dtype` (gated: `int gate, int dtype`) before the stream.
+for _name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
+              "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd"):
+    _res, _args = _SIGS[_name]
+    _extra = [_INT, _INT] if "gated" in _name else [_INT]
+    _SIGS[_name + "_ex"] = (_res, _args[:-1] + _extra + [_P])
+del _name, _res, _args, _extra
 
 _lock = threading.Lock()
 _lib: Optional[ctypes.CDLL] = None
@@ -113,9 +130,9 @@ def _ptr(t: Optional[torch.Tensor]):
     return None if t is None else ctypes.c_void_p(t.data_ptr())
 
 
-def _act(t: torch.Tensor, name: str, T: int, D: int) -> int:
-    if t.dtype != torch.bfloat16 or not t.is_cuda or t.dim() != 2:
-        raise TypeError(f"{name}: expected a 2-D bf16 CUDA tensor, got {t.dtype} {t.device} {tuple(t.shape)}")
+def _act(t: torch.Tensor, name: str, T: int, D: int, dtype: torch.dtype = torch.bfloat16) -> int:
+    if t.dtype != dtype or not t.is_cuda or t.dim() != 2:
+        raise TypeError(f"{name}: expected a 2-D {dtype} CUDA tensor, got {t.dtype} {t.device} {tuple(t.shape)}")
     if tuple(t.shape) != (T, D):
         raise ValueError(f"{name}: expected shape {(T, D)}, got {tuple(t.shape)}")
     if D > 1 and t.stride(1) != 1:
@@ -137,6 +154,18 @@ def _stream(stream, dev) -> ctypes.c_void_p:
 def _check(fn: str, status: int):
     if status != 0:
         raise RmsNormError(fn, status)
+
+
+def _dtype_code(x: torch.Tensor) -> int:
+    if x.dtype not in DTYPE_CODES:
+        raise TypeError(f"activations must be bf16 or fp16, got {x.dtype}")
+    return DTYPE_CODES[x.dtype]
+
+
+def _gate_code(gate: str) -> int:
+    if gate not in GATE_CODES:
+        raise ValueError(f"gate must be one of {sorted(GATE_CODES)}, got {gate!r}")
+    return GATE_CODES[gate]
 
 
 def _ws(ws: torch.Tensor):
@@ -303,6 +332,121 @@ def rmsnorm_gated_bwd_recompute(g, x, z, w, rstd, dx, dz, dw, y, ws, zero_center
     _check("rmsnorm_gated_bwd_recompute", load().rmsnorm_gated_bwd_recompute(
         _ptr(g), ldg, _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dz), lddz, _ptr(dw),
         _ptr(y), ldy, wp, wb, T, D, int(zero_centered_gamma), _stream(stream, x.device)))
+
+
+# --------------------------------------------------------------------------
+# activation dtype (bf16 / fp16, from x) and gate (silu / sigmoid) options
+# --------------------------------------------------------------------------
+def rmsnorm_fwd_ex(x, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: bool = False, stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldx, ldy = _act(x, "x", T, D, dt), _act(y, "y", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_fwd_ex", load().rmsnorm_fwd_ex(
+        _ptr(x), ldx, _ptr(w), _ptr(y), ldy, _ptr(rstd), T, D, float(eps), int(zero_centered_gamma),
+        _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_bwd_ex(g, x, w, rstd, dx, dgamma, ws, zero_centered_gamma: bool = False, stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldg, ldx, lddx = _act(g, "g", T, D, dt), _act(x, "x", T, D, dt), _act(dx, "dx", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_bwd_ex", load().rmsnorm_bwd_ex(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dgamma), wp, wb, T, D,
+        int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_residual_fwd_ex(x, w, y, rstd, x_copy, eps: float = 1e-6, zero_centered_gamma: bool = False,
+                            stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldx, ldy, ldc = _act(x, "x", T, D, dt), _act(y, "y", T, D, dt), _act(x_copy, "x_copy", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_residual_fwd_ex", load().rmsnorm_residual_fwd_ex(
+        _ptr(x), ldx, _ptr(w), _ptr(y), ldy, _ptr(rstd), _ptr(x_copy), ldc, T, D, float(eps),
+        int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_residual_bwd_ex(g, x, w, rstd, g_res, dx, dgamma, ws, zero_centered_gamma: bool = False,
+                            stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldg, ldx, lddx = _act(g, "g", T, D, dt), _act(x, "x", T, D, dt), _act(dx, "dx", T, D, dt)
+    ldgr = _act(g_res, "g_res", T, D, dt) if g_res is not None else D
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_residual_bwd_ex", load().rmsnorm_residual_bwd_ex(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dx), lddx, _ptr(dgamma),
+        wp, wb, T, D, int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_fwd_ex(x, z, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: bool = True,
+                         gate: str = "silu", stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldx, ldz, ldy = _act(x, "x", T, D, dt), _act(z, "z", T, D, dt), _act(y, "y", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_gated_fwd_ex", load().rmsnorm_gated_fwd_ex(
+        _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(y), ldy, _ptr(rstd), T, D, float(eps),
+        int(zero_centered_gamma), _gate_code(gate), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_bwd_ex(g, x, z, w, rstd, dx, dz, dw, ws, zero_centered_gamma: bool = True,
+                         gate: str = "silu", stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldg, ldx, ldz = _act(g, "g", T, D, dt), _act(x, "x", T, D, dt), _act(z, "z", T, D, dt)
+    lddx, lddz = _act(dx, "dx", T, D, dt), _act(dz, "dz", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dw is not None:
+        _f32(dw, "dw", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_gated_bwd_ex", load().rmsnorm_gated_bwd_ex(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dz), lddz,
+        _ptr(dw), wp, wb, T, D, int(zero_centered_gamma), _gate_code(gate), _dtype_code(x),
+        _stream(stream, x.device)))
+
+
+def rmsnorm_fused_add_fwd_ex(x, res, w, y, rstd, res_out, eps: float = 1e-6, zero_centered_gamma: bool = False,
+                             stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldx, ldr = _act(x, "x", T, D, dt), _act(res, "res", T, D, dt)
+    ldy, ldo = _act(y, "y", T, D, dt), _act(res_out, "res_out", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    _check("rmsnorm_fused_add_fwd_ex", load().rmsnorm_fused_add_fwd_ex(
+        _ptr(x), ldx, _ptr(res), ldr, _ptr(w), _ptr(y), ldy, _ptr(rstd), _ptr(res_out), ldo, T, D, float(eps),
+        int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_fused_add_bwd_ex(g, x, res, w, rstd, g_res, dh, dgamma, ws, zero_centered_gamma: bool = False,
+                             stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldg, ldx = _act(g, "g", T, D, dt), _act(x, "x", T, D, dt)
+    ldr, ldd = _act(res, "res", T, D, dt), _act(dh, "dh", T, D, dt)
+    ldgr = _act(g_res, "g_res", T, D, dt) if g_res is not None else D
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_fused_add_bwd_ex", load().rmsnorm_fused_add_bwd_ex(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(res), ldr, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dh), ldd,
+        _ptr(dgamma), wp, wb, T, D, int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
 
 
 def rmsnorm_dgamma_reduce(ws, T: int, D: int, dgamma, stream=None):

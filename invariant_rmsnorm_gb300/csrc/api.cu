@@ -163,20 +163,200 @@ inline int cuda_status(cudaError_t e) { return e == cudaSuccess ? RMSN_OK : RMSN
 
 float inv_pow2(int D) { return (D & (D - 1)) == 0 ? 1.0f / static_cast<float>(D) : 0.0f; }
 
-int run_fwd(Mode m, FwdArgs a, cudaStream_t s) {
+// Variant flags of an activation dtype / gate argument (RMSN_EINVAL if unknown).
+int dtype_flags(int dtype, int* flags) {
+    if (dtype == RMSN_DTYPE_BF16) { *flags = 0; return RMSN_OK; }
+    if (dtype == RMSN_DTYPE_F16) { *flags = kFlagF16; return RMSN_OK; }
+    return RMSN_EINVAL;
+}
+
+int gate_flags(int gate, int* flags) {
+    if (gate == RMSN_GATE_SILU) { *flags = 0; return RMSN_OK; }
+    if (gate == RMSN_GATE_SIGMOID) { *flags = kFlagSigmoid; return RMSN_OK; }
+    return RMSN_EINVAL;
+}
+
+// `m` = Mode | variant flags.
+int run_fwd(int m, FwdArgs a, cudaStream_t s) {
     a.inv_d_pow2 = inv_pow2(a.D);
     const RowCfg c = row_cfg(a.D);
-    const cudaError_t e = c.narrow ? launch_narrow_fwd(m, a, c, s) : launch_wide_fwd(m, a, c, s);
+    cudaError_t e;
+    if (is_f16(m)) e = c.narrow ? launch_narrow_fwd_f16(m, a, c, s) : launch_wide_fwd_f16(m, a, c, s);
+    else e = c.narrow ? launch_narrow_fwd(m, a, c, s) : launch_wide_fwd(m, a, c, s);
     return cuda_status(e);
 }
 
-int run_bwd(Mode m, BwdArgs a, float* dgamma, cudaStream_t s) {
+int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     a.inv_d_pow2 = inv_pow2(a.D);
     const RowCfg c = row_cfg(a.D);
-    cudaError_t e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);
+    cudaError_t e;
+    if (is_f16(m)) e = c.narrow ? launch_narrow_bwd_f16(m, a, c, s) : launch_wide_bwd_f16(m, a, c, s);
+    else e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);
     if (e != cudaSuccess) return RMSN_ECUDA;
     if (dgamma != nullptr) e = launch_dgamma_reduce(a.partials, num_chunks(a.T, a.D), a.D, dgamma, s);
     return cuda_status(e);
+}
+
+}  // namespace
+
+// ---------------------------------------------------------------------------
+// The operations, with the variant flags (activation dtype, gate) as the first
+// argument; the entry points below validate those and call these.
+// ---------------------------------------------------------------------------
+namespace {
+
+int rmsnorm_fwd_impl(int flags, const rmsn_act16* x, int64_t ldx, const float* w, rmsn_act16* y, int64_t ldy,
+                     float* rstd, int64_t T, int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kPlain | flags, a, stream);
+}
+
+int rmsnorm_residual_fwd_impl(int flags, const rmsn_act16* x, int64_t ldx, const float* w, rmsn_act16* y,
+                              int64_t ldy, float* rstd, rmsn_act16* x_copy, int64_t ldxc, int64_t T, int64_t D,
+                              float eps, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_act(x_copy, ldxc, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd; a.xc = x_copy; a.ldxc = ldxc;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kResidual | flags, a, stream);
+}
+
+int rmsnorm_gated_fwd_impl(int flags, const rmsn_act16* x, int64_t ldx, const rmsn_act16* z, int64_t ldz,
+                           const float* w, rmsn_act16* y, int64_t ldy, float* rstd, int64_t T, int64_t D, float eps,
+                           int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kGated | flags, a, stream);
+}
+
+int rmsnorm_bwd_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx, const float* w,
+                     const float* rstd, rmsn_act16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes,
+                     int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.w = w; a.rstd = rstd; a.dx = dx; a.lddx = lddx;
+    a.partials = static_cast<float*>(ws); a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(kPlain | flags, a, dgamma, stream);
+}
+
+int rmsnorm_residual_bwd_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                              const float* w, const float* rstd, const rmsn_act16* g_res, int64_t ldgr,
+                              rmsn_act16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes, int64_t T,
+                              int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    // A zero residual gradient is the plain backward.
+    return run_bwd((g_res ? kResidual : kPlain) | flags, a, dgamma, stream);
+}
+
+int rmsnorm_gated_bwd_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                           const rmsn_act16* z, int64_t ldz, const float* w, const float* rstd, rmsn_act16* dx,
+                           int64_t lddx, rmsn_act16* dz, int64_t lddz, float* dw, void* ws, size_t ws_bytes,
+                           int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_act(dz, lddz, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dw) RMSN_TRY(check_vec(dw));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.dz = dz; a.lddz = lddz; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(kGated | flags, a, dw, stream);
+}
+
+int rmsnorm_fused_add_fwd_impl(int flags, const rmsn_act16* x, int64_t ldx, const rmsn_act16* res, int64_t ldres,
+                               const float* w, rmsn_act16* y, int64_t ldy, float* rstd, rmsn_act16* res_out,
+                               int64_t ldro, int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                               rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(res, ldres, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_act(res_out, ldro, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    RMSN_TRY(check_eps(eps));
+    FwdArgs a{};
+    a.x = x; a.ldx = ldx; a.res = res; a.ldres = ldres; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
+    a.xc = res_out; a.ldxc = ldro;
+    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
+    return run_fwd(kFusedAdd | flags, a, stream);
+}
+
+int rmsnorm_fused_add_bwd_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                               const rmsn_act16* res, int64_t ldres, const float* w, const float* rstd,
+                               const rmsn_act16* g_res, int64_t ldgr, rmsn_act16* dh, int64_t lddh, float* dgamma,
+                               void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma,
+                               rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(res, ldres, D));
+    RMSN_TRY(check_act(dh, lddh, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.res = res; a.ldres = ldres; a.gres = g_res; a.ldgr = ldgr;
+    a.w = w; a.rstd = rstd; a.dx = dh; a.lddx = lddh; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd((g_res ? kFusedAdd : kFusedAddNoGres) | flags, a, dgamma, stream);
 }
 
 }  // namespace
@@ -203,53 +383,49 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t D) {
     return static_cast<size_t>(num_chunks(T, static_cast<int>(D))) * static_cast<size_t>(D) * 4u;
 }
 
-int rmsnorm_fwd(const rmsn_bf16* x, int64_t ldx, const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
-                int64_t T, int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(y, ldy, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    RMSN_TRY(check_eps(eps));
-    FwdArgs a{};
-    a.x = x; a.ldx = ldx; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
-    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
-    return run_fwd(kPlain, a, stream);
+int rmsnorm_fwd(const rmsn_bf16* x, int64_t ldx, const float* w, rmsn_bf16* y, int64_t ldy, float* rstd, int64_t T,
+                int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream) {
+    return rmsnorm_fwd_impl(0, x, ldx, w, y, ldy, rstd, T, D, eps, zero_centered_gamma, stream);
 }
 
-int rmsnorm_residual_fwd(const rmsn_bf16* x, int64_t ldx, const float* w, rmsn_bf16* y, int64_t ldy,
-                         float* rstd, rmsn_bf16* x_copy, int64_t ldxc, int64_t T, int64_t D, float eps,
-                         int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(y, ldy, D));
-    RMSN_TRY(check_act(x_copy, ldxc, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    RMSN_TRY(check_eps(eps));
-    FwdArgs a{};
-    a.x = x; a.ldx = ldx; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd; a.xc = x_copy; a.ldxc = ldxc;
-    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
-    return run_fwd(kResidual, a, stream);
+int rmsnorm_fwd_ex(const rmsn_act16* x, int64_t ldx, const float* w, rmsn_act16* y, int64_t ldy, float* rstd,
+                   int64_t T, int64_t D, float eps, int zero_centered_gamma, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_fwd_impl(f, x, ldx, w, y, ldy, rstd, T, D, eps, zero_centered_gamma, stream);
+}
+
+int rmsnorm_residual_fwd(const rmsn_bf16* x, int64_t ldx, const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
+                         rmsn_bf16* x_copy, int64_t ldxc, int64_t T, int64_t D, float eps, int zero_centered_gamma,
+                         rmsn_stream stream) {
+    return rmsnorm_residual_fwd_impl(0, x, ldx, w, y, ldy, rstd, x_copy, ldxc, T, D, eps, zero_centered_gamma,
+                                     stream);
+}
+
+int rmsnorm_residual_fwd_ex(const rmsn_act16* x, int64_t ldx, const float* w, rmsn_act16* y, int64_t ldy,
+                            float* rstd, rmsn_act16* x_copy, int64_t ldxc, int64_t T, int64_t D, float eps,
+                            int zero_centered_gamma, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_residual_fwd_impl(f, x, ldx, w, y, ldy, rstd, x_copy, ldxc, T, D, eps, zero_centered_gamma,
+                                     stream);
 }
 
 int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz, const float* w,
                       rmsn_bf16* y, int64_t ldy, float* rstd, int64_t T, int64_t D, float eps,
                       int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(z, ldz, D));
-    RMSN_TRY(check_act(y, ldy, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    RMSN_TRY(check_eps(eps));
-    FwdArgs a{};
-    a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
-    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
-    return run_fwd(kGated, a, stream);
+    return rmsnorm_gated_fwd_impl(0, x, ldx, z, ldz, w, y, ldy, rstd, T, D, eps, zero_centered_gamma, stream);
+}
+
+int rmsnorm_gated_fwd_ex(const rmsn_act16* x, int64_t ldx, const rmsn_act16* z, int64_t ldz, const float* w,
+                         rmsn_act16* y, int64_t ldy, float* rstd, int64_t T, int64_t D, float eps,
+                         int zero_centered_gamma, int gate, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    int fg = 0;
+    RMSN_TRY(gate_flags(gate, &fg));
+    f |= fg;
+    return rmsnorm_gated_fwd_impl(f, x, ldx, z, ldz, w, y, ldy, rstd, T, D, eps, zero_centered_gamma, stream);
 }
 
 int rmsnorm_gated_hf_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz, const float* w,
@@ -269,107 +445,94 @@ int rmsnorm_gated_hf_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, in
     return run_fwd(kGatedHF, a, stream);
 }
 
-int rmsnorm_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
-                const float* rstd, rmsn_bf16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes,
-                int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(dx, lddx, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dgamma) RMSN_TRY(check_vec(dgamma));
-    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
-    BwdArgs a{};
-    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.w = w; a.rstd = rstd; a.dx = dx; a.lddx = lddx;
-    a.partials = static_cast<float*>(ws); a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
-    return run_bwd(kPlain, a, dgamma, stream);
+int rmsnorm_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w, const float* rstd,
+                rmsn_bf16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                int zero_centered_gamma, rmsn_stream stream) {
+    return rmsnorm_bwd_impl(0, g, ldg, x, ldx, w, rstd, dx, lddx, dgamma, ws, ws_bytes, T, D, zero_centered_gamma,
+                            stream);
+}
+
+int rmsnorm_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx, const float* w,
+                   const float* rstd, rmsn_act16* dx, int64_t lddx, float* dgamma, void* ws, size_t ws_bytes,
+                   int64_t T, int64_t D, int zero_centered_gamma, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_bwd_impl(f, g, ldg, x, ldx, w, rstd, dx, lddx, dgamma, ws, ws_bytes, T, D, zero_centered_gamma,
+                            stream);
 }
 
 int rmsnorm_residual_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
                          const float* rstd, const rmsn_bf16* g_res, int64_t ldgr, rmsn_bf16* dx, int64_t lddx,
-                         float* dgamma, void* ws, size_t ws_bytes, int64_t T, int64_t D,
-                         int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(dx, lddx, D));
-    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dgamma) RMSN_TRY(check_vec(dgamma));
-    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
-    BwdArgs a{};
-    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
-    a.dx = dx; a.lddx = lddx; a.partials = static_cast<float*>(ws);
-    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
-    // A zero residual gradient is the plain backward.
-    return run_bwd(g_res ? kResidual : kPlain, a, dgamma, stream);
+                         float* dgamma, void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma,
+                         rmsn_stream stream) {
+    return rmsnorm_residual_bwd_impl(0, g, ldg, x, ldx, w, rstd, g_res, ldgr, dx, lddx, dgamma, ws, ws_bytes, T, D,
+                                     zero_centered_gamma, stream);
+}
+
+int rmsnorm_residual_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx, const float* w,
+                            const float* rstd, const rmsn_act16* g_res, int64_t ldgr, rmsn_act16* dx, int64_t lddx,
+                            float* dgamma, void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma,
+                            int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_residual_bwd_impl(f, g, ldg, x, ldx, w, rstd, g_res, ldgr, dx, lddx, dgamma, ws, ws_bytes, T, D,
+                                     zero_centered_gamma, stream);
 }
 
 int rmsnorm_gated_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z,
                       int64_t ldz, const float* w, const float* rstd, rmsn_bf16* dx, int64_t lddx, rmsn_bf16* dz,
                       int64_t lddz, float* dw, void* ws, size_t ws_bytes, int64_t T, int64_t D,
                       int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(z, ldz, D));
-    RMSN_TRY(check_act(dx, lddx, D));
-    RMSN_TRY(check_act(dz, lddz, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dw) RMSN_TRY(check_vec(dw));
-    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
-    BwdArgs a{};
-    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.rstd = rstd;
-    a.dx = dx; a.lddx = lddx; a.dz = dz; a.lddz = lddz; a.partials = static_cast<float*>(ws);
-    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
-    return run_bwd(kGated, a, dw, stream);
+    return rmsnorm_gated_bwd_impl(0, g, ldg, x, ldx, z, ldz, w, rstd, dx, lddx, dz, lddz, dw, ws, ws_bytes, T, D,
+                                  zero_centered_gamma, stream);
+}
+
+int rmsnorm_gated_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx, const rmsn_act16* z,
+                         int64_t ldz, const float* w, const float* rstd, rmsn_act16* dx, int64_t lddx,
+                         rmsn_act16* dz, int64_t lddz, float* dw, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                         int zero_centered_gamma, int gate, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    int fg = 0;
+    RMSN_TRY(gate_flags(gate, &fg));
+    f |= fg;
+    return rmsnorm_gated_bwd_impl(f, g, ldg, x, ldx, z, ldz, w, rstd, dx, lddx, dz, lddz, dw, ws, ws_bytes, T, D,
+                                  zero_centered_gamma, stream);
 }
 
 int rmsnorm_fused_add_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* res, int64_t ldres, const float* w,
                           rmsn_bf16* y, int64_t ldy, float* rstd, rmsn_bf16* res_out, int64_t ldro, int64_t T,
                           int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(res, ldres, D));
-    RMSN_TRY(check_act(y, ldy, D));
-    RMSN_TRY(check_act(res_out, ldro, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    RMSN_TRY(check_eps(eps));
-    FwdArgs a{};
-    a.x = x; a.ldx = ldx; a.res = res; a.ldres = ldres; a.w = w; a.y = y; a.ldy = ldy; a.rstd = rstd;
-    a.xc = res_out; a.ldxc = ldro;
-    a.T = T; a.D = static_cast<int>(D); a.eps = eps; a.zc = zero_centered_gamma ? 1 : 0;
-    return run_fwd(kFusedAdd, a, stream);
+    return rmsnorm_fused_add_fwd_impl(0, x, ldx, res, ldres, w, y, ldy, rstd, res_out, ldro, T, D, eps,
+                                      zero_centered_gamma, stream);
+}
+
+int rmsnorm_fused_add_fwd_ex(const rmsn_act16* x, int64_t ldx, const rmsn_act16* res, int64_t ldres, const float* w,
+                             rmsn_act16* y, int64_t ldy, float* rstd, rmsn_act16* res_out, int64_t ldro, int64_t T,
+                             int64_t D, float eps, int zero_centered_gamma, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_fused_add_fwd_impl(f, x, ldx, res, ldres, w, y, ldy, rstd, res_out, ldro, T, D, eps,
+                                      zero_centered_gamma, stream);
 }
 
 int rmsnorm_fused_add_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* res,
                           int64_t ldres, const float* w, const float* rstd, const rmsn_bf16* g_res, int64_t ldgr,
                           rmsn_bf16* dh, int64_t lddh, float* dgamma, void* ws, size_t ws_bytes, int64_t T,
                           int64_t D, int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(res, ldres, D));
-    RMSN_TRY(check_act(dh, lddh, D));
-    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dgamma) RMSN_TRY(check_vec(dgamma));
-    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
-    BwdArgs a{};
-    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.res = res; a.ldres = ldres; a.gres = g_res; a.ldgr = ldgr;
-    a.w = w; a.rstd = rstd; a.dx = dh; a.lddx = lddh; a.partials = static_cast<float*>(ws);
-    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
-    return run_bwd(g_res ? kFusedAdd : kFusedAddNoGres, a, dgamma, stream);
+    return rmsnorm_fused_add_bwd_impl(0, g, ldg, x, ldx, res, ldres, w, rstd, g_res, ldgr, dh, lddh, dgamma, ws,
+                                      ws_bytes, T, D, zero_centered_gamma, stream);
+}
+
+int rmsnorm_fused_add_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                             const rmsn_act16* res, int64_t ldres, const float* w, const float* rstd,
+                             const rmsn_act16* g_res, int64_t ldgr, rmsn_act16* dh, int64_t lddh, float* dgamma,
+                             void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma, int dtype,
+                             rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_fused_add_bwd_impl(f, g, ldg, x, ldx, res, ldres, w, rstd, g_res, ldgr, dh, lddh, dgamma, ws,
+                                      ws_bytes, T, D, zero_centered_gamma, stream);
 }
 
 int rmsnorm_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const float* w,
@@ -394,7 +557,8 @@ int rmsnorm_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, i
     return run_bwd(g_res ? kResidual : kPlain, a, dgamma, stream);
 }
 
-int rmsnorm_gated_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z,
+int rmsnorm_gated_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
+                                const rmsn_bf16* z,
                                 int64_t ldz, const float* w, const float* rstd, rmsn_bf16* dx, int64_t lddx,
                                 rmsn_bf16* dz, int64_t lddz, float* dw, rmsn_bf16* y, int64_t ldy, void* ws,
                                 size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
@@ -433,6 +597,8 @@ int rmsnorm_device_error(unsigned int* flags, int clear) {
     cudaError_t e = cudaDeviceSynchronize();
     if (e == cudaSuccess) e = wide_read_error(flags, clear != 0);
     if (e == cudaSuccess) e = narrow_read_error(flags, clear != 0);
+    if (e == cudaSuccess) e = wide_f16_read_error(flags, clear != 0);
+    if (e == cudaSuccess) e = narrow_f16_read_error(flags, clear != 0);
     return cuda_status(e);
 }
 

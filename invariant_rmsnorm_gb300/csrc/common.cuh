@@ -1,6 +1,7 @@
 // Shared device-side building blocks for the sm_103a RMSNorm kernels:
-// inline-PTX wrappers for mbarriers, bulk (TMA) copies and cp.async, bf16
-// packing, separately rounded fp32 arithmetic, and the fixed butterfly sum.
+// inline-PTX wrappers for mbarriers, bulk (TMA) copies and cp.async, bf16 and
+// fp16 packing, separately rounded fp32 arithmetic, the gate functions, and
+// the fixed butterfly sum.
 //
 // Every wait on an mbarrier is bounded: a waiter that sees no progress for
 // kWaitTimeoutNs of global time gives up and reports failure, and the kernels
@@ -9,6 +10,7 @@
 
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -210,6 +212,40 @@ __device__ __forceinline__ uint4 pack8(const float f[8]) {
     return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// fp16 <-> fp32: exact widening; round-to-nearest-even narrowing (subnormals
+// kept, overflow to infinity).
+__device__ __forceinline__ void unpack8_f16(const uint4 v, float f[8]) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const float2 t = __half22float2(*reinterpret_cast<const __half2*>(&w[i]));  // .x = low half
+        f[2 * i] = t.x;
+        f[2 * i + 1] = t.y;
+    }
+}
+
+__device__ __forceinline__ uint4 pack8_f16(const float f[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        __half2 h = __floats2half2_rn(f[2 * i], f[2 * i + 1]);
+        w[i] = *reinterpret_cast<uint32_t*>(&h);
+    }
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Eight activations of the kernel's storage format (fp16 if F16, else bf16).
+template <bool F16>
+__device__ __forceinline__ void unpack_act(const uint4 v, float f[8]) {
+    if constexpr (F16) unpack8_f16(v, f);
+    else unpack8(v, f);
+}
+template <bool F16>
+__device__ __forceinline__ uint4 pack_act(const float f[8]) {
+    if constexpr (F16) return pack8_f16(f);
+    else return pack8(f);
+}
+
 // An fp32 value rounded to bf16 (nearest even) and widened back.
 __device__ __forceinline__ float round_bf16f(float v) { return __bfloat162float(__float2bfloat16_rn(v)); }
 
@@ -230,6 +266,29 @@ __device__ __forceinline__ float sigmoidf_rn(float z) {
     const float e = __expf(-fabsf(z));
     const float s = __fdividef(1.0f, fadd(1.0f, e));
     return z >= 0.0f ? s : fmul(e, s);
+}
+
+// The gate q(z) of the gated norm and its derivative, from one exponential:
+//   silu:    q = z sigmoid(z),  q' = sigmoid(z) (1 + z (1 - sigmoid(z)))
+//   sigmoid: q = sigmoid(z),    q' = sigmoid(z) sigmoid(-z) = e s^2
+// (with e, s as in sigmoidf_rn; the product form has no cancellation in
+// either tail, where 1 - sigmoid(z) would lose every bit for z >> 0).
+template <bool SIG>
+__device__ __forceinline__ float gate_value(float z) {
+    return SIG ? sigmoidf_rn(z) : fmul(z, sigmoidf_rn(z));
+}
+template <bool SIG>
+__device__ __forceinline__ void gate_eval(float z, float& q, float& dq) {
+    const float e = __expf(-fabsf(z));
+    const float s = __fdividef(1.0f, fadd(1.0f, e));
+    const float sg = z >= 0.0f ? s : fmul(e, s);
+    if (SIG) {
+        q = sg;
+        dq = fmul(e, fmul(s, s));
+    } else {
+        q = fmul(z, sg);
+        dq = fmul(sg, fadd(1.0f, fmul(z, fsub(1.0f, sg))));
+    }
 }
 
 // x / D, correctly rounded. When D is a power of two the host passes its exact

@@ -14,15 +14,33 @@ namespace rmsn {
 // weight multiply); forward only.
 enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2, kFusedAdd = 3, kFusedAddNoGres = 4, kGatedHF = 5 };
 
-__host__ __device__ constexpr bool is_fused(int mode) { return mode == kFusedAdd || mode == kFusedAddNoGres; }
-__host__ __device__ constexpr bool is_gated(int mode) { return mode == kGated || mode == kGatedHF; }
+// Variant flags OR-ed into a mode (the kernels' MODE template argument):
+// fp16 activations instead of bf16, and for kGated the sigmoid gate instead of
+// silu. The arithmetic between load and store is the same fp32 in every case.
+constexpr int kModeMask = 0xff;
+constexpr int kFlagF16 = 0x100;
+constexpr int kFlagSigmoid = 0x200;
+
+__host__ __device__ constexpr int base_mode(int mode) { return mode & kModeMask; }
+__host__ __device__ constexpr bool is_f16(int mode) { return (mode & kFlagF16) != 0; }
+__host__ __device__ constexpr bool is_sigmoid_gate(int mode) { return (mode & kFlagSigmoid) != 0; }
+__host__ __device__ constexpr bool is_fused(int mode) {
+    return base_mode(mode) == kFusedAdd || base_mode(mode) == kFusedAddNoGres;
+}
+__host__ __device__ constexpr bool is_gated(int mode) {
+    return base_mode(mode) == kGated || base_mode(mode) == kGatedHF;
+}
 
 // Operands streamed per row, by mode.
 __host__ __device__ constexpr int fwd_inputs(int mode) { return (is_gated(mode) || is_fused(mode)) ? 2 : 1; }
 __host__ __device__ constexpr int bwd_inputs(int mode) {
-    return mode == kPlain ? 2 : (mode == kResidual || mode == kGated || mode == kFusedAddNoGres) ? 3 : 4;
+    return base_mode(mode) == kPlain ? 2
+           : (base_mode(mode) == kResidual || base_mode(mode) == kGated || base_mode(mode) == kFusedAddNoGres) ? 3
+                                                                                                                : 4;
 }
-__host__ __device__ constexpr bool has_gres(int mode) { return mode == kResidual || mode == kFusedAdd; }
+__host__ __device__ constexpr bool has_gres(int mode) {
+    return base_mode(mode) == kResidual || base_mode(mode) == kFusedAdd;
+}
 
 // Everything a forward launch needs (unused pointers are null).
 struct FwdArgs {
@@ -72,10 +90,16 @@ int narrow_stage_rows_for_group(int G);
 int64_t num_chunks(int64_t T, int D);
 
 // Launchers (return the launch's cudaError_t; arguments already validated).
-cudaError_t launch_wide_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
-cudaError_t launch_wide_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
-cudaError_t launch_narrow_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
-cudaError_t launch_narrow_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
+// `m` is a Mode with its variant flags. The bf16 variants are instantiated in
+// wide.cu / narrow.cu, the fp16 ones in wide_f16.cu / narrow_f16.cu.
+cudaError_t launch_wide_fwd(int m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_wide_bwd(int m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_narrow_fwd(int m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_narrow_bwd(int m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_wide_fwd_f16(int m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_wide_bwd_f16(int m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_narrow_fwd_f16(int m, const FwdArgs& a, const RowCfg& c, cudaStream_t s);
+cudaError_t launch_narrow_bwd_f16(int m, const BwdArgs& a, const RowCfg& c, cudaStream_t s);
 cudaError_t launch_dgamma_reduce(const float* partials, int64_t nchunks, int D, float* out,
                                  cudaStream_t s);
 
@@ -87,11 +111,14 @@ int ctas_per_sm(const void* kernel, int threads, int smem_bytes);
 // Error-word access for each kernel translation unit.
 cudaError_t wide_read_error(unsigned* flags, bool clear);
 cudaError_t narrow_read_error(unsigned* flags, bool clear);
+cudaError_t wide_f16_read_error(unsigned* flags, bool clear);
+cudaError_t narrow_f16_read_error(unsigned* flags, bool clear);
 
 // Tensor-map encoding through the driver entry point (no libcuda link needed).
-// Rows of bf16: box = [box_rows][D]. Vector of fp32: box = [box].
+// Rows of 16-bit activations (bf16, or fp16 if `f16`): box = [box_rows][D].
+// Vector of fp32: box = [box].
 cudaError_t encode_rows_2d(CUtensorMap* map, const void* base, int64_t T, int D, int64_t ld_elems,
-                           int box_rows);
+                           int box_rows, bool f16);
 cudaError_t encode_vec_1d(CUtensorMap* map, const float* base, int64_t T, int box);
 
 }  // namespace rmsn

@@ -1,704 +1,31 @@
-// Wide-row kernels (D > 256): a CTA reduces R whole rows per iteration.
-//
-// Design (GB300, HBM-bound):
-//   * Persistent grid: at most (SM count x resident CTAs) CTAs, each walking a
-//     fixed sequence of rows (forward) or of whole row chunks (backward).
-//   * Warp-specialised pipeline. The last warp of the CTA is a producer: one
-//     lane keeps S stages of R rows in flight with 1-D bulk TMA copies
-//     (cp.async.bulk global->shared, completion counted on a per-stage "full"
-//     mbarrier). The consumer warps read a stage into registers and release it
-//     on its "empty" mbarrier (one arrive per warp) before they reduce, so the
-//     producer refills it while the arithmetic runs and no consumer ever
-//     waits for a copy to be issued.
-//   * Consumer thread t owns VPT 16-byte vectors of each row at slots
-//     v = k*NT + t (coalesced, conflict-free shared reads).
-//   * Fixed reduction tree (a function of D only): per-thread ascending sum
-//     over its slots and the 8 lanes of each vector, an xor-butterfly over the
-//     warp (offsets 16..1), then the per-warp totals added in warp order. The
-//     R rows of an iteration share one named barrier but each keeps its own
-//     tree, so a row's bits depend on nothing but the row and D: not on T, its
-//     position, the other rows, the grid or the GPU.
-//   * fp32 arithmetic with every multiply and add rounded separately (no FMA
-//     contraction), rsqrtf for the inverse RMS, bf16 round-to-nearest-even
-//     outputs written with 128-bit streaming stores.
-//   * Backward weight gradient: a CTA owns whole chunks of kWideChunkRows rows,
-//     accumulates g*x*r per column in ascending row order in registers and
-//     writes one fp32 partial row per chunk; no atomics anywhere.
-//   * Every mbarrier wait is bounded; a consumer that gives up votes through the
-//     reduction barrier, the CTA stops, the device error flag is raised, and no
-//     thread leaves while a copy it issued can still land.
-//
-// Sources: Megatron-LM pull request 6859 "Fix the batch-invariant RMSNorm
-// forward and its input gradient" (What does this PR do, items 1-2);
-// RL-Kernel pull request 414 "[DSv4][P1-5] rmsnorm_residual" (Implementation:
-// rsqrt, (x*r)*gamma, ascending fp32 reductions, separate rounding, no atomics;
-// Summary: the residual variant returns a copy of x); RL-Kernel pull request
-// 467 "...zero-centred RMSNorm references and CUDA kernel" (+1 in fp32, gated
-// norm with the weight multiply in fp32).
-#include <algorithm>
-
-#include "common.cuh"
-#include "kernels.h"
-
-// Launch shapes, chosen by measurement on GB300 (T=32768, D=4096): the
-// forward runs 3 CTAs of 96 KB rings per SM; the backward 2 CTAs of 64 KB.
-#ifndef RMSN_WIDE_FWD_SMEM
-#define RMSN_WIDE_FWD_SMEM (96 * 1024)   // target ring bytes per CTA (forward)
-#endif
-#ifndef RMSN_WIDE_FWD_CTAS_PER_SM
-#define RMSN_WIDE_FWD_CTAS_PER_SM 3
-#endif
-#ifndef RMSN_WIDE_BWD_SMEM
-#define RMSN_WIDE_BWD_SMEM (64 * 1024)   // target ring bytes per CTA (backward)
-#endif
-#ifndef RMSN_WIDE_BWD_CTAS_PER_SM
-#define RMSN_WIDE_BWD_CTAS_PER_SM 2
-#endif
-#ifndef RMSN_MAX_STAGES
-#define RMSN_MAX_STAGES 16
-#endif
-#ifndef RMSN_FWD_ROWS
-#define RMSN_FWD_ROWS 4   // rows per forward iteration
-#endif
-#ifndef RMSN_BWD_ROWS
-#define RMSN_BWD_ROWS 2   // rows per backward iteration (divides the chunk)
-#endif
-#ifndef RMSN_BWD_LEAN
-#define RMSN_BWD_LEAN 1   // backward recomputes products after the reduction (fewer registers)
-#endif
-#ifndef RMSN_BWD_MINB
-#define RMSN_BWD_MINB 2   // backward CTAs that must fit on one SM (register budget)
-#endif
+// Wide-row kernels (D > 256) with bf16 activations: the instantiations of
+// wide_impl.cuh for every bf16 mode, and their launch entry points.
+#include "wide_impl.cuh"
 
 namespace rmsn {
 
-// Rows per iteration. Larger rows need no batching, and R > 1 would overflow
-// registers (a 9-warp CTA puts 3 warps on one scheduler: <= 168 registers per
-// thread) or shared memory.
-template <int VPT> __host__ __device__ constexpr int fwd_rows() { return VPT >= 4 ? 1 : RMSN_FWD_ROWS; }
-template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_rows() {
-    return (VPT == 1 && MAXT <= 256) ? RMSN_BWD_ROWS : 1;
-}
+cudaError_t wide_read_error(unsigned* flags, bool clear) { return read_wide_error_word(flags, clear); }
 
-constexpr int kConsumerBarrier = 1;  // named barrier id of the consumer warps
-
-static __device__ unsigned int g_wide_error;
-
-cudaError_t wide_read_error(unsigned* flags, bool clear) {
-    unsigned v = 0;
-    cudaError_t e = cudaMemcpyFromSymbol(&v, g_wide_error, sizeof(v));
-    if (e != cudaSuccess) return e;
-    *flags |= v;
-    if (clear && v) {
-        const unsigned zero = 0;
-        e = cudaMemcpyToSymbol(g_wide_error, &zero, sizeof(zero));
-    }
-    return e;
-}
-
-namespace {
-
-// Load this thread's effective weights: w, or w + 1 in fp32 (zero-centred gamma).
-template <int VPT>
-__device__ __forceinline__ void load_weights(const float* w, int zc, int NV, int nt, int tid,
-                                             float (&we)[VPT][8]) {
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = k * nt + tid;
-        if (v < NV) {
-            const float4 lo = __ldg(reinterpret_cast<const float4*>(w) + 2 * v);
-            const float4 hi = __ldg(reinterpret_cast<const float4*>(w) + 2 * v + 1);
-            we[k][0] = lo.x; we[k][1] = lo.y; we[k][2] = lo.z; we[k][3] = lo.w;
-            we[k][4] = hi.x; we[k][5] = hi.y; we[k][6] = hi.z; we[k][7] = hi.w;
-            if (zc) {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) we[k][e] = fadd(we[k][e], 1.0f);
-            }
-        } else {
-#pragma unroll
-            for (int e = 0; e < 8; ++e) we[k][e] = 0.0f;
-        }
-    }
-}
-
-// The values a row is normalised over: x, or the fp32 sum x + res (fused add).
-template <int MODE>
-__device__ __forceinline__ void norm_input(const uint4 xv, const uint4 sv, float (&f)[8]) {
-    unpack8(xv, f);
-    if (is_fused(MODE)) {
-        float rv[8];
-        unpack8(sv, rv);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) f[e] = fadd(f[e], rv[e]);
-    }
-}
-
-// First half of the block-wide fixed tree, for R rows at once: butterfly
-// within each consumer warp (the R chains interleave), lane 0 parks each warp
-// total in red[r*32 + warp]. The consumers' named barrier doubles as the error
-// vote: returns the AND of every consumer's `ok`.
-template <int R>
-__device__ __forceinline__ int block_partial(float (&v)[R], float* red, int lane, int warp, int nt, bool ok) {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-#pragma unroll
-        for (int r = 0; r < R; ++r) v[r] = fadd(v[r], __shfl_xor_sync(0xffffffffu, v[r], o));
-    if (lane == 0) {
-#pragma unroll
-        for (int r = 0; r < R; ++r) red[r * 32 + warp] = v[r];
-    }
-    return named_bar_and(kConsumerBarrier, nt, ok ? 1 : 0);
-}
-
-// Second half: the warp totals added in warp order (same bits in every thread).
-// All loads are issued before the dependent adds.
-template <int NWMAX>
-__device__ __forceinline__ float block_total(const float* red, int nw) {
-    float w[NWMAX];
-#pragma unroll
-    for (int i = 0; i < NWMAX; ++i) w[i] = (i < nw) ? red[i] : 0.0f;
-    float t = w[0];
-#pragma unroll
-    for (int i = 1; i < NWMAX; ++i)
-        if (i < nw) t = fadd(t, w[i]);
-    return t;
-}
-
-// Producer loop (one lane): fill stage i % S with iteration i once the
-// consumers have released the iteration S earlier. `issue(i)` posts the copies.
-// If the consumers stop releasing (a consumer gave up), wait (bounded) for the
-// copies still in flight, raise the flag and stop.
-// Stage index and phase parity advance together (no divisions on the hot path).
-template <typename Issue>
-__device__ __forceinline__ void produce(uint64_t* full, uint64_t* empty, int S, int n_it, Issue&& issue) {
-    int s = 0;
-    uint32_t ph = 0;
-    for (int i = 0; i < n_it; ++i) {
-        if (i >= S && !mbar_wait(&empty[s], ph ^ 1u)) {
-            for (int j = i - S; j < i; ++j) (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1));
-            atomicOr(&g_wide_error, kErrWaitTimeout);
-            return;
-        }
-        fence_proxy_async_smem();
-        issue(i, s);
-        if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-        }
-    }
-}
-
-// A consumer gave up at iteration i: one thread waits (bounded) for the stages
-// the producer may still be filling, then raises the flag.
-__device__ void consumer_abort(uint64_t* full, int S, int i, int n_it) {
-    for (int j = i; j < n_it && j < i + S; ++j) (void)mbar_wait(&full[j % S], static_cast<uint32_t>((j / S) & 1));
-    atomicOr(&g_wide_error, kErrWaitTimeout);
-}
-
-}  // namespace
-
-// ---------------------------------------------------------------------------
-// Forward: plain / zero-centred, residual (adds the copy), gated (reads z).
-// Stage layout [row][x | z][D]. blockDim = NT consumers + 32 (producer warp).
-// ---------------------------------------------------------------------------
-template <int VPT, int MODE, int MAXT>
-__global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, const int S) {
-    constexpr int NIN = fwd_inputs(MODE);
-    constexpr int R = fwd_rows<VPT>();
-    constexpr int NWMAX = MAXT / 32;
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int D = a.D;
-    const int NV = D >> 3;
-    const int nt = blockDim.x - 32;  // consumer threads
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-    const int64_t T = a.T;
-    const int64_t G = gridDim.x;
-    const int64_t cta = blockIdx.x;
-    const uint32_t row_bytes = static_cast<uint32_t>(D) * 2u;
-    const uint32_t stage_bytes = R * NIN * row_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
-    uint64_t* empty = full + S;
-    float* red = reinterpret_cast<float*>(empty + S);  // [2][R][32]
-
-    const int n_my = (cta < T) ? static_cast<int>((T - 1 - cta) / G + 1) : 0;  // rows cta, cta+G, ...
-    const int n_it = (n_my + R - 1) / R;
-
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], nw);
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == nw) {  // producer warp
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            produce(full, empty, S, n_it, [&](int i, int s) {
-                unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
-                const int nvalid = min(n_my - i * R, R);
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nvalid) * NIN * row_bytes);
-                for (int r = 0; r < nvalid; ++r) {
-                    const int64_t row = cta + static_cast<int64_t>(i * R + r) * G;
-                    unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
-                    bulk_g2s(dst, a.x + row * a.ldx, row_bytes, &full[s], pol);
-                    if (is_gated(MODE)) bulk_g2s(dst + row_bytes, a.z + row * a.ldz, row_bytes, &full[s], pol);
-                    if (is_fused(MODE)) bulk_g2s(dst + row_bytes, a.res + row * a.ldres, row_bytes, &full[s], pol);
-                }
-            });
-        }
-        return;
-    }
-
-    float we[VPT][8];
-    load_weights<VPT>(a.w, a.zc, NV, nt, tid, we);
-
-    int s = 0;
-    uint32_t ph = 0;
-    for (int i = 0; i < n_it; ++i) {
-        const bool ok = mbar_wait(&full[s], ph);
-        const unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
-        const int nvalid = min(n_my - i * R, R);
-
-        uint4 xv[R][VPT];
-        uint4 zv[R][VPT];  // gated: z; fused add: res
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (r < nvalid) {
-                const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_bytes;
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    const int v = j * nt + tid;
-                    if (v < NV) {
-                        xv[r][j] = ld_shared_v4(src + 16 * v);
-                        if (NIN == 2) zv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
-                    }
-                }
-            }
-        }
-        // The stage is in registers: hand it back to the producer.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-        }
-
-        float ss[R];
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            ss[r] = 0.0f;
-            if (r < nvalid) {
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    if (j * nt + tid < NV) {
-                        float f[8];
-                        norm_input<MODE>(xv[r][j], zv[r][j], f);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) ss[r] = fadd(ss[r], fmul(f[e], f[e]));
-                    }
-                }
-            }
-        }
-        float* rb = red + (i & 1) * (R * 32);
-        if (!block_partial<R>(ss, rb, lane, warp, nt, ok)) {
-            if (tid == 0) consumer_abort(full, S, i, n_it);
-            return;
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (r < nvalid) {
-                const float tot = block_total<NWMAX>(rb + r * 32, nw);
-                const float rr = rsqrtf(fadd(div_by_d(tot, D, a.inv_d_pow2), a.eps));
-                const int64_t row = cta + static_cast<int64_t>(i * R + r) * G;
-                if (tid == 0) a.rstd[row] = rr;
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    const int v = j * nt + tid;
-                    if (v < NV) {
-                        float f[8], o[8];
-                        norm_input<MODE>(xv[r][j], zv[r][j], f);
-                        if (MODE == kGated) {
-                            float zf[8];
-                            unpack8(zv[r][j], zf);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float q = fmul(zf[e], sigmoidf_rn(zf[e]));
-                                o[e] = fmul(fmul(fmul(f[e], rr), we[j][e]), q);
-                            }
-                        } else if (MODE == kGatedHF) {
-                            // HF convention: normalised value and weight multiply in bf16.
-                            float zf[8];
-                            unpack8(zv[r][j], zf);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float n = round_bf16f(fmul(f[e], rr));
-                                const float t = round_bf16f(fmul(round_bf16f(we[j][e]), n));
-                                o[e] = fmul(t, fmul(zf[e], sigmoidf_rn(zf[e])));
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = fmul(fmul(f[e], rr), we[j][e]);
-                        }
-                        st_global_cs(a.y + row * a.ldy + 8 * v, pack8(o));
-                        if (MODE == kResidual) st_global_cs(a.xc + row * a.ldxc + 8 * v, xv[r][j]);
-                        if (is_fused(MODE)) st_global_cs(a.xc + row * a.ldxc + 8 * v, pack8(f));  // bf16(x + res)
-                    }
-                }
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Backward pass 1: dx (and dz), plus one weight-gradient partial per chunk.
-// Each iteration handles R consecutive rows of one chunk (R divides the chunk
-// size, so an iteration never straddles two chunks). Stage layout
-// [row][g | x | g_res or z][D]; each row's rstd arrives in the same stage
-// through a 4-byte cp.async, and one no-increment arrive after them makes the
-// stage's full barrier (expected count 2) wait for those copies too.
-// The products needed after the row reduction (g*w_eff, x, g*x; gated: with
-// g*silu(z) for g) are computed once before it and kept in registers.
-// ---------------------------------------------------------------------------
-template <int VPT, int MODE, int MAXT>
-__global__ void __launch_bounds__(MAXT + 32, ((MAXT <= 256 && VPT <= 2) ? RMSN_BWD_MINB : 1))
-wide_bwd_kernel(const BwdArgs a, const int S) {
-    constexpr int NIN = bwd_inputs(MODE);
-    constexpr int C = kWideChunkRows;
-    constexpr int R = bwd_rows<VPT, MAXT>();
-    constexpr int NWMAX = MAXT / 32;
-    static_assert(C % R == 0, "rows per iteration must divide the chunk");
-    extern __shared__ __align__(128) unsigned char smem[];
-    const int D = a.D;
-    const int NV = D >> 3;
-    const int nt = blockDim.x - 32;  // consumer threads
-    const int tid = threadIdx.x;
-    const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
-    const int64_t T = a.T;
-    const int64_t G = gridDim.x;
-    const int64_t cta = blockIdx.x;
-    const int64_t nchunks = (T + C - 1) / C;
-    const uint32_t row_bytes = static_cast<uint32_t>(D) * 2u;
-    const uint32_t stage_bytes = R * NIN * row_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
-    uint64_t* empty = full + S;
-    float* rs = reinterpret_cast<float*>(empty + S);  // [S][R]
-    float* red = rs + S * R;                          // [2][R][32]
-
-    // This CTA's chunks: cta, cta+G, ...; only the globally last chunk can be
-    // short, and if this CTA owns it, it is its last one.
-    int n_my = 0;
-    if (cta < nchunks) {
-        const int64_t cnt = (nchunks - 1 - cta) / G + 1;
-        const int64_t last = cta + (cnt - 1) * G;
-        const int64_t last_rows = (T - last * C) < C ? (T - last * C) : C;
-        n_my = static_cast<int>((cnt - 1) * C + last_rows);
-    }
-    const int n_it = (n_my + R - 1) / R;
-    // k-th row of this CTA (C is a power of two: shifts, no divisions).
-    auto row_of = [&](int k) -> int64_t { return (cta + static_cast<int64_t>(k / C) * G) * C + (k % C); };
-
-    if (tid == 0) {
-        for (int s = 0; s < S; ++s) {
-            mbar_init(&full[s], 2);
-            mbar_init(&empty[s], nw);
-        }
-        fence_mbar_init();
-    }
-    __syncthreads();
-
-    if (warp == nw) {  // producer warp
-        if (lane == 0) {
-            const uint64_t pol = policy_evict_first();
-            // Operands after g and x: residual g_res; gated z; fused add res, then g_res.
-            const uint16_t* third = (MODE == kResidual) ? a.gres : (MODE == kGated ? a.z : a.res);
-            const int64_t ld_third = (MODE == kResidual) ? a.ldgr : (MODE == kGated ? a.ldz : a.ldres);
-            produce(full, empty, S, n_it, [&](int i, int s) {
-                unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
-                const int nvalid = min(n_my - i * R, R);
-                mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nvalid) * NIN * row_bytes);
-                for (int r = 0; r < nvalid; ++r) cp_async4(&rs[s * R + r], a.rstd + row_of(i * R + r));
-                cp_async_arrive_noinc(&full[s]);
-                for (int r = 0; r < nvalid; ++r) {
-                    const int64_t row = row_of(i * R + r);
-                    unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
-                    bulk_g2s(dst, a.g + row * a.ldg, row_bytes, &full[s], pol);
-                    bulk_g2s(dst + row_bytes, a.x + row * a.ldx, row_bytes, &full[s], pol);
-                    if (NIN >= 3)
-                        bulk_g2s(dst + 2 * row_bytes, third + row * ld_third, row_bytes, &full[s], pol);
-                    if (NIN == 4) bulk_g2s(dst + 3 * row_bytes, a.gres + row * a.ldgr, row_bytes, &full[s], pol);
-                }
-            });
-        }
-        return;
-    }
-
-    float we[VPT][8];
-    load_weights<VPT>(a.w, a.zc, NV, nt, tid, we);
-    float acc[VPT][8];
-#pragma unroll
-    for (int j = 0; j < VPT; ++j)
-#pragma unroll
-        for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
-
-    int s = 0;
-    uint32_t ph = 0;
-    for (int i = 0; i < n_it; ++i) {
-        const bool ok = mbar_wait(&full[s], ph);
-        const unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
-        const int nvalid = min(n_my - i * R, R);
-
-        float gw[R][VPT][8];  // g*w_eff   (gated: g*silu(z)*w_eff)
-        float xs[R][VPT][8];  // x
-        float gx[R][VPT][8];  // g*x       (gated: g*silu(z)*x)
-        float tz[R][VPT][8];  // residual: g_res; gated: z; fused add: res
-        float g0[R][VPT][8];  // gated: g
-        float rr[R];
-        float sp[R];          // this thread's part of s = sum g x w_eff (gated: g q x w_eff)
-        uint4 gv[R][VPT], xv[R][VPT], tv[R][VPT], fv[R][VPT];  // fv: fused add's g_res
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            rr[r] = 0.0f;
-            if (r < nvalid) {
-                rr[r] = rs[s * R + r];
-                const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_bytes;
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    const int v = j * nt + tid;
-                    if (v < NV) {
-                        gv[r][j] = ld_shared_v4(src + 16 * v);
-                        xv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
-                        if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_bytes + 16 * v);
-                        if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
-                    }
-                }
-            }
-        }
-        // The stage is in registers: hand it back to the producer.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
-        if (++s == S) {
-            s = 0;
-            ph ^= 1u;
-        }
-
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            sp[r] = 0.0f;
-            if (r < nvalid) {
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    if (j * nt + tid < NV) {
-                        float gf[8];
-                        unpack8(gv[r][j], gf);
-                        norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);  // x, or h = x + res
-                        if (MODE == kResidual || MODE == kGated) unpack8(tv[r][j], tz[r][j]);
-                        if (MODE == kGated) {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                g0[r][j][e] = gf[e];
-                                gf[e] = fmul(gf[e], fmul(tz[r][j][e], sigmoidf_rn(tz[r][j][e])));  // g*silu(z)
-                            }
-                        }
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            gw[r][j][e] = fmul(gf[e], we[j][e]);
-                            if (!RMSN_BWD_LEAN) gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
-                            sp[r] = fadd(sp[r], fmul(gw[r][j][e], xs[r][j][e]));
-                        }
-                    }
-                }
-            }
-        }
-        float* rb = red + (i & 1) * (R * 32);
-        if (!block_partial<R>(sp, rb, lane, warp, nt, ok)) {
-            if (tid == 0) consumer_abort(full, S, i, n_it);
-            return;
-        }
-#pragma unroll
-        for (int r = 0; r < R; ++r) {
-            if (r < nvalid) {
-                const float r1 = rr[r];
-                const float s_tot = block_total<NWMAX>(rb + r * 32, nw);
-                const float coef = fmul(div_by_d(fmul(fmul(r1, r1), r1), D, a.inv_d_pow2), s_tot);
-                const int64_t row = row_of(i * R + r);
-                uint16_t* dxrow = a.dx + row * a.lddx;
-#pragma unroll
-                for (int j = 0; j < VPT; ++j) {
-                    const int v = j * nt + tid;
-                    if (v < NV) {
-                        if (RMSN_BWD_LEAN) {
-                            // Recompute the phase-1 products from the packed row (same bits).
-                            float gf[8];
-                            unpack8(gv[r][j], gf);
-                            norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
-                            if (MODE == kResidual || MODE == kGated) unpack8(tv[r][j], tz[r][j]);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                if (MODE == kGated) {
-                                    g0[r][j][e] = gf[e];
-                                    gf[e] = fmul(gf[e], fmul(tz[r][j][e], sigmoidf_rn(tz[r][j][e])));
-                                }
-                                gw[r][j][e] = fmul(gf[e], we[j][e]);
-                                gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
-                            }
-                        }
-                        float o[8], fg[8];
-                        if (MODE == kFusedAdd) unpack8(fv[r][j], fg);
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            float d = fsub(fmul(gw[r][j][e], r1), fmul(xs[r][j][e], coef));
-                            if (MODE == kResidual) d = fadd(d, tz[r][j][e]);
-                            if (MODE == kFusedAdd) d = fadd(d, fg[e]);
-                            o[e] = d;
-                            acc[j][e] = fadd(acc[j][e], fmul(gx[r][j][e], r1));
-                        }
-                        st_global_cs(dxrow + 8 * v, pack8(o));
-                        if (MODE == kGated) {
-                            float dzv[8], yv[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                const float z = tz[r][j][e];
-                                const float sg = sigmoidf_rn(z);
-                                const float u = fmul(fmul(xs[r][j][e], r1), we[j][e]);
-                                const float dsilu = fmul(sg, fadd(1.0f, fmul(z, fsub(1.0f, sg))));
-                                dzv[e] = fmul(fmul(g0[r][j][e], u), dsilu);
-                                yv[e] = fmul(u, fmul(z, sg));
-                            }
-                            st_global_cs(a.dz + row * a.lddz + 8 * v, pack8(dzv));
-                            if (a.y) st_global_cs(a.y + row * a.ldy + 8 * v, pack8(yv));
-                        } else if (a.y) {
-                            // The forward output again, from the saved rstd: same operations,
-                            // same bits as the forward's y.
-                            float yv[8];
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), we[j][e]);
-                            st_global_cs(a.y + row * a.ldy + 8 * v, pack8(yv));
-                        }
-                    }
-                }
-            }
-        }
-        // End of a chunk: write its partial row and restart the accumulators.
-        const int k_last = i * R + nvalid - 1;
-        if ((k_last % C) == C - 1 || k_last == n_my - 1) {
-            const int64_t chunk = cta + static_cast<int64_t>(k_last / C) * G;
-            float* prow = a.partials + chunk * D;
-            // Partials are re-read by pass 2 right away: keep them in L2.
-            const uint64_t keep = policy_evict_last();
-#pragma unroll
-            for (int j = 0; j < VPT; ++j) {
-                const int v = j * nt + tid;
-                if (v < NV) {
-                    st_global_f4_hint(prow + 8 * v, acc[j][0], acc[j][1], acc[j][2], acc[j][3], keep);
-                    st_global_f4_hint(prow + 8 * v + 4, acc[j][4], acc[j][5], acc[j][6], acc[j][7], keep);
-                }
-#pragma unroll
-                for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
-            }
-        }
-    }
-}
-
-// ---------------------------------------------------------------------------
-// Launchers
-// ---------------------------------------------------------------------------
-namespace {
-
-constexpr int kMaxSmemPerCta = 227 * 1024;
-
-inline int stages_for(size_t budget, size_t stage_bytes, size_t per_stage_extra, size_t fixed) {
-    size_t s = budget / stage_bytes;
-    if (s > RMSN_MAX_STAGES) s = RMSN_MAX_STAGES;
-    while (s > 2 && s * (stage_bytes + per_stage_extra) + fixed > static_cast<size_t>(kMaxSmemPerCta)) --s;
-    if (s < 2) s = 2;
-    return static_cast<int>(s);
-}
-
-template <int VPT, int MODE, int MAXT>
-cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
-    constexpr int NIN = fwd_inputs(MODE);
-    constexpr int R = fwd_rows<VPT>();
-    const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
-    const size_t fixed = 2 * R * 32 * 4;
-    const int S = stages_for(RMSN_WIDE_FWD_SMEM, stage, 16, fixed);
-    const size_t smem = S * (stage + 16) + fixed;
-    if (smem > static_cast<size_t>(kMaxSmemPerCta)) return cudaErrorInvalidConfiguration;
-    const int threads = c.threads + 32;
-    const void* kern = reinterpret_cast<const void*>(wide_fwd_kernel<VPT, MODE, MAXT>);
-    cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), RMSN_WIDE_FWD_CTAS_PER_SM);
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int64_t grid = std::min<int64_t>(a.T, static_cast<int64_t>(sm_count()) * occ);
-    wide_fwd_kernel<VPT, MODE, MAXT><<<static_cast<unsigned>(grid), threads, smem, st>>>(a, S);
-    return cudaGetLastError();
-}
-
-template <int VPT, int MODE, int MAXT>
-cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
-    constexpr int NIN = bwd_inputs(MODE);
-    constexpr int R = bwd_rows<VPT, MAXT>();
-    const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
-    const size_t fixed = 2 * R * 32 * 4;
-    const int S = stages_for(RMSN_WIDE_BWD_SMEM, stage, 16 + 4 * R, fixed);
-    const size_t smem = S * (stage + 16 + 4 * R) + fixed;
-    if (smem > static_cast<size_t>(kMaxSmemPerCta)) return cudaErrorInvalidConfiguration;
-    const int threads = c.bwd_threads + 32;
-    const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT>);
-    cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), RMSN_WIDE_BWD_CTAS_PER_SM);
-    if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int64_t nchunks = (a.T + kWideChunkRows - 1) / kWideChunkRows;
-    const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
-    wide_bwd_kernel<VPT, MODE, MAXT><<<static_cast<unsigned>(grid), threads, smem, st>>>(a, S);
-    return cudaGetLastError();
-}
-
-template <int MODE>
-cudaError_t fwd_dispatch(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
-    const bool big = c.threads > 256;
-    switch (c.vpt) {
-        case 1: return big ? fwd_t<1, MODE, 512>(a, c, st) : fwd_t<1, MODE, 256>(a, c, st);
-        case 2: return big ? fwd_t<2, MODE, 512>(a, c, st) : fwd_t<2, MODE, 256>(a, c, st);
-        case 4: return big ? fwd_t<4, MODE, 512>(a, c, st) : fwd_t<4, MODE, 256>(a, c, st);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <int MODE>
-cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
-    const bool big = c.bwd_threads > 256;
-    switch (c.bwd_vpt) {
-        case 1: return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
-        case 2: return big ? bwd_t<2, MODE, 512>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
-        case 4: return big ? bwd_t<4, MODE, 512>(a, c, st) : bwd_t<4, MODE, 256>(a, c, st);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-}  // namespace
-
-cudaError_t launch_wide_fwd(Mode m, const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
+cudaError_t launch_wide_fwd(int m, const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
     switch (m) {
         case kPlain: return fwd_dispatch<kPlain>(a, c, st);
         case kResidual: return fwd_dispatch<kResidual>(a, c, st);
         case kGated: return fwd_dispatch<kGated>(a, c, st);
+        case kGated | kFlagSigmoid: return fwd_dispatch<kGated | kFlagSigmoid>(a, c, st);
         case kFusedAdd:
         case kFusedAddNoGres: return fwd_dispatch<kFusedAdd>(a, c, st);
         case kGatedHF: return fwd_dispatch<kGatedHF>(a, c, st);
+        default: break;
     }
     return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_wide_bwd(Mode m, const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
+cudaError_t launch_wide_bwd(int m, const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     switch (m) {
         case kPlain: return bwd_dispatch<kPlain>(a, c, st);
         case kResidual: return bwd_dispatch<kResidual>(a, c, st);
         case kGated: return bwd_dispatch<kGated>(a, c, st);
+        case kGated | kFlagSigmoid: return bwd_dispatch<kGated | kFlagSigmoid>(a, c, st);
         case kFusedAdd: return bwd_dispatch<kFusedAdd>(a, c, st);
         case kFusedAddNoGres: return bwd_dispatch<kFusedAddNoGres>(a, c, st);
         default: break;

@@ -33,10 +33,16 @@ def _gen(seed: int, device) -> torch.Generator:
 
 def normal_bf16(shape, seed: int, device="cpu", std: float = 1.0) -> torch.Tensor:
     """bf16 tensor of N(0, std^2) draws (drawn in fp32, rounded by torch to bf16)."""
+    return normal16(shape, seed, device, std, torch.bfloat16)
+
+
+def normal16(shape, seed: int, device="cpu", std: float = 1.0, dtype=torch.bfloat16) -> torch.Tensor:
+    """16-bit (bf16 or fp16) tensor of N(0, std^2) draws: the same fp32 draws
+    for either format, rounded by torch."""
     x = torch.randn(shape, generator=_gen(seed, device), device=device, dtype=torch.float32)
     if std != 1.0:
         x = x * std
-    return x.to(torch.bfloat16)
+    return x.to(dtype)
 
 
 def gamma_f32(D: int, seed: int, device="cpu", mean: float = 1.0, std: float = 0.1) -> torch.Tensor:

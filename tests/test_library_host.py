@@ -88,6 +88,27 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.rmsnorm_device_error(None, 0) == -1
 
 
+def test_ex_options_are_validated_on_the_host(lib):
+    """Unknown activation formats and gates are rejected before anything else;
+    known ones reach the ordinary validation (here: a null input)."""
+    A = 1 << 20
+    fwd = lambda dt, x=A: lib.rmsnorm_fwd_ex(x, 128, A, A, 128, A, 4, 128, 1e-6, 0, dt, None)
+    assert fwd(2) == -1 and fwd(-1) == -1
+    assert fwd(0, x=0) == -1 and fwd(1, x=0) == -1
+    assert fwd(1, x=A + 2) == -2
+    gfwd = lambda gate, dt=0: lib.rmsnorm_gated_fwd_ex(A, 128, A, 128, A, A, 128, A, 4, 128, 1e-6, 1, gate, dt,
+                                                       None)
+    assert gfwd(2) == -1 and gfwd(0, dt=3) == -1
+    need = rn.rmsnorm_bwd_workspace_bytes(4, 128)
+    assert lib.rmsnorm_gated_bwd_ex(A, 128, A, 128, A, 128, A, A, A, 128, A, 128, A, None, need, 4, 128, 1,
+                                    1, 1, None) == -5
+    assert lib.rmsnorm_gated_bwd_ex(A, 128, A, 128, A, 128, A, A, A, 128, A, 128, A, A, need, 4, 128, 1,
+                                    5, 1, None) == -1
+    assert lib.rmsnorm_fused_add_bwd_ex(A, 128, A, 128, A, 128, A, A, None, 128, A, 128, A, A, need, 4, 128,
+                                        0, 9, None) == -1
+    assert lib.rmsnorm_residual_fwd_ex(0, 0, 0, 0, 0, 0, 0, 0, 0, 128, 1e-6, 0, 1, None) == 0  # T = 0
+
+
 def test_package_has_no_non_cuda_path():
     """The binding refuses to run without the built library (no fallback)."""
     import importlib
