@@ -14,6 +14,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <utility>
+
 #include "rmsnorm.h"
 
 namespace rmsn {
@@ -35,6 +37,53 @@ constexpr int kReduceWarps = 32;         // weight-gradient pass 2: warps (chunk
 constexpr unsigned kErrWaitTimeout = 1u;
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch. Every kernel is launched with programmatic
+// stream serialization allowed (launch_kernel below), so it may become
+// resident while the previous kernel of its stream drains. It runs only its
+// prologue (shared-memory barriers; no global memory), then waits in
+// pdl_wait() until that kernel has completed and its memory is visible. Each
+// CTA calls pdl_release() once its main loop is done, so the next kernel of
+// the stream starts launching when every CTA is in its epilogue: its launch
+// latency and prologue overlap this kernel's end, while its CTAs still land on
+// SMs that are (almost) free, as in an ordinary launch. Kernels launched
+// without the attribute see both as no-ops.
+// ---------------------------------------------------------------------------
+#ifndef RMSN_PDL
+#define RMSN_PDL 1
+#endif
+
+__device__ __forceinline__ void pdl_wait() {
+#if RMSN_PDL
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+#endif
+}
+
+__device__ __forceinline__ void pdl_release() {
+#if RMSN_PDL
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+#endif
+}
+
+// Launch `kern` on `st` (programmatic stream serialization allowed when
+// RMSN_PDL is set). Returns the launch's error.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                          Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = RMSN_PDL ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
 
 // ---------------------------------------------------------------------------
 // PTX wrappers

@@ -175,6 +175,7 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // first global memory access below
 
     if (warp == kNarrowThreads / 32) {  // producer warp
         if (lane == 0) {
@@ -262,6 +263,7 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
             ph ^= 1u;
         }
     }
+    pdl_release();
 }
 
 // ---------------------------------------------------------------------------
@@ -315,6 +317,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // first global memory access below
 
     if (warp == kNarrowThreads / 32) {  // producer warp
         if (lane == 0) {
@@ -448,6 +451,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
             cbuf ^= 1;
         }
     }
+    pdl_release();
 }
 
 // ---------------------------------------------------------------------------
@@ -486,8 +490,7 @@ cudaError_t nfwd_t(const FwdArgs& a, cudaStream_t st) {
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nblocks = (a.T + RS - 1) / RS;
     const int64_t grid = std::min<int64_t>(nblocks, static_cast<int64_t>(sm_count()) * occ);
-    narrow_fwd_kernel<MODE, G><<<static_cast<unsigned>(grid), threads, smem, st>>>(a, m, S);
-    return cudaGetLastError();
+    return launch_kernel(narrow_fwd_kernel<MODE, G>, static_cast<unsigned>(grid), threads, smem, st, a, m, S);
 }
 
 template <int MODE, int G>
@@ -521,8 +524,7 @@ cudaError_t nbwd_t(const BwdArgs& a, cudaStream_t st) {
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nchunks = (a.T + CN - 1) / CN;
     const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
-    narrow_bwd_kernel<MODE, G><<<static_cast<unsigned>(grid), threads, smem, st>>>(a, m, S);
-    return cudaGetLastError();
+    return launch_kernel(narrow_bwd_kernel<MODE, G>, static_cast<unsigned>(grid), threads, smem, st, a, m, S);
 }
 
 template <int MODE>

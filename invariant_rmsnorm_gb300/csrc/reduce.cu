@@ -25,6 +25,7 @@ constexpr int kUnroll = RMSN_REDUCE_UNROLL;  // loads in flight per lane
 __global__ void __launch_bounds__(32 * kReduceWarps)
 dgamma_reduce_kernel(const float* __restrict__ partials, int64_t nchunks, int D, float* __restrict__ out) {
     __shared__ float tot[kReduceWarps][32];
+    pdl_wait();
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int col = blockIdx.x * 32 + lane;
     const int64_t per = (nchunks + kReduceWarps - 1) / kReduceWarps;
@@ -43,6 +44,7 @@ dgamma_reduce_kernel(const float* __restrict__ partials, int64_t nchunks, int D,
         }
         for (; c < c1; ++c) acc = fadd(acc, __ldcs(p + c * D));
     }
+    pdl_release();
     tot[warp][lane] = acc;
     __syncthreads();
     if (warp == 0 && col < D) {
@@ -55,8 +57,7 @@ dgamma_reduce_kernel(const float* __restrict__ partials, int64_t nchunks, int D,
 
 cudaError_t launch_dgamma_reduce(const float* partials, int64_t nchunks, int D, float* out, cudaStream_t s) {
     const unsigned grid = static_cast<unsigned>((D + 31) / 32);
-    dgamma_reduce_kernel<<<grid, 32 * kReduceWarps, 0, s>>>(partials, nchunks, D, out);
-    return cudaGetLastError();
+    return launch_kernel(dgamma_reduce_kernel, grid, 32 * kReduceWarps, 0, s, partials, nchunks, D, out);
 }
 
 }  // namespace rmsn

@@ -239,6 +239,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // first global memory access below
 
     if (warp == nw) {  // producer warp
         if (lane == 0) {
@@ -357,6 +358,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
             }
         }
     }
+    pdl_release();
 }
 
 // ---------------------------------------------------------------------------
@@ -418,6 +420,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         fence_mbar_init();
     }
     __syncthreads();
+    pdl_wait();  // first global memory access below
 
     if (warp == nw) {  // producer warp
         if (lane == 0) {
@@ -609,6 +612,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             }
         }
     }
+    pdl_release();
 }
 
 // ---------------------------------------------------------------------------
@@ -641,8 +645,7 @@ cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), RMSN_WIDE_FWD_CTAS_PER_SM);
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t grid = std::min<int64_t>(a.T, static_cast<int64_t>(sm_count()) * occ);
-    wide_fwd_kernel<VPT, MODE, MAXT><<<static_cast<unsigned>(grid), threads, smem, st>>>(a, S);
-    return cudaGetLastError();
+    return launch_kernel(wide_fwd_kernel<VPT, MODE, MAXT>, static_cast<unsigned>(grid), threads, smem, st, a, S);
 }
 
 template <int VPT, int MODE, int MAXT>
@@ -662,8 +665,7 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nchunks = (a.T + kWideChunkRows - 1) / kWideChunkRows;
     const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
-    wide_bwd_kernel<VPT, MODE, MAXT><<<static_cast<unsigned>(grid), threads, smem, st>>>(a, S);
-    return cudaGetLastError();
+    return launch_kernel(wide_bwd_kernel<VPT, MODE, MAXT>, static_cast<unsigned>(grid), threads, smem, st, a, S);
 }
 
 template <int MODE>
