@@ -32,17 +32,23 @@
 #include "common.cuh"
 #include "kernels.h"
 
+// Launch shapes, chosen by measurement on GB300 (262144 x 128 gated): 4
+// forward CTAs of 48 KB rings per SM, 3 backward CTAs of 48 KB rings (plus the
+// chunk combine buffer) with at most 72 registers per thread.
 #ifndef RMSN_NARROW_FWD_SMEM
-#define RMSN_NARROW_FWD_SMEM (64 * 1024)
+#define RMSN_NARROW_FWD_SMEM (48 * 1024)
 #endif
 #ifndef RMSN_NARROW_FWD_CTAS_PER_SM
-#define RMSN_NARROW_FWD_CTAS_PER_SM 3
+#define RMSN_NARROW_FWD_CTAS_PER_SM 4
 #endif
 #ifndef RMSN_NARROW_BWD_SMEM
-#define RMSN_NARROW_BWD_SMEM (96 * 1024)
+#define RMSN_NARROW_BWD_SMEM (48 * 1024)
 #endif
 #ifndef RMSN_NARROW_BWD_CTAS_PER_SM
-#define RMSN_NARROW_BWD_CTAS_PER_SM 2
+#define RMSN_NARROW_BWD_CTAS_PER_SM 3
+#endif
+#ifndef RMSN_NARROW_BWD_MINB
+#define RMSN_NARROW_BWD_MINB 3  // backward CTAs that must fit on one SM (register budget)
 #endif
 
 namespace rmsn {
@@ -90,9 +96,14 @@ constexpr int kNarrowConsumerBarrier = 1;
 // Rows of one pass (P), of one stage (RS) and of one weight-gradient chunk (CN).
 template <int G> __host__ __device__ constexpr int narrow_pass_rows() { return kNarrowThreads / G; }
 // Rows of 256 B < 2D <= 512 B use 32-row stages so that two stages of four
-// operands still fit in shared memory; narrower rows use 64 (or P).
+// operands still fit in shared memory; narrower rows use RMSN_NARROW_STAGE_ROWS
+// (or P). The stage size does not enter any reduction tree.
+#ifndef RMSN_NARROW_STAGE_ROWS
+#define RMSN_NARROW_STAGE_ROWS 32
+#endif
 template <int G> __host__ __device__ constexpr int narrow_stage_rows() {
-    return G == 32 ? 32 : (narrow_pass_rows<G>() > 64 ? narrow_pass_rows<G>() : 64);
+    return G == 32 ? 32
+                   : (narrow_pass_rows<G>() > RMSN_NARROW_STAGE_ROWS ? narrow_pass_rows<G>() : RMSN_NARROW_STAGE_ROWS);
 }
 template <int G> __host__ __device__ constexpr int narrow_chunk_rows() {
     return narrow_stage_rows<G>() > kNarrowChunkRowsMin ? narrow_stage_rows<G>() : kNarrowChunkRowsMin;
@@ -270,7 +281,7 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
 // Backward pass 1. Stage = RS rows of g, x (and g_res or z) plus their rstd.
 // ---------------------------------------------------------------------------
 template <int MODE, int G>
-__global__ void __launch_bounds__(kNarrowThreads + 32)
+__global__ void __launch_bounds__(kNarrowThreads + 32, RMSN_NARROW_BWD_MINB)
 narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const int S) {
     constexpr int M = base_mode(MODE);
     constexpr bool F16 = is_f16(MODE);
