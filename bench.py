@@ -208,9 +208,11 @@ def run_ours(args):
         step()
     torch.cuda.synchronize()
 
-    # Per-kernel events bracket every 4th step only (each record adds a small
-    # gap between kernels); the step time comes from the events around the loop.
-    sampled = list(range(0, args.steps, 4))
+    # Per-kernel events bracket every 16th step only: an event recorded between
+    # two kernels adds a small gap and stops the second from launching while
+    # the first drains (programmatic dependent launch), so the sampled steps
+    # run a little slower. The step time comes from the events around the loop.
+    sampled = list(range(0, args.steps, 16))
     evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for k in sampled}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     gpu_id = "0"

@@ -305,15 +305,46 @@ __device__ __forceinline__ float fmul(float a, float b) { return __fmul_rn(a, b)
 __device__ __forceinline__ float fadd(float a, float b) { return __fadd_rn(a, b); }
 __device__ __forceinline__ float fsub(float a, float b) { return __fsub_rn(a, b); }
 
+// e^-a for a >= 0, from the PTX instruction ex2.approx.ftz.f32 (2^x, which
+// flushes subnormal results to zero): e^-a = 2^t with t = -a log2(e). For
+// t < -64 the argument is raised by 64 and the result scaled back by an exact
+// multiply with 2^-64, so results down to the smallest fp32 subnormal (reached
+// at a of about 103) are kept rather than flushed. Relative error about
+// (2 + 2a) * 2^-24: 2 ulp from the instruction, the rest from rounding t.
+#ifndef RMSN_FAST_EXP
+#define RMSN_FAST_EXP 1
+#endif
+__device__ __forceinline__ float exp_neg(float a) {
+#if RMSN_FAST_EXP
+    const float t = fmul(a, -1.4426950408889634f);
+    const bool low = t < -64.0f;
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(low ? fadd(t, 64.0f) : t));
+    return low ? fmul(r, 5.42101086242752217e-20f) : r;
+#else
+    return __expf(-a);
+#endif
+}
+
+// 1 / d for d in [1, 2] (never subnormal, so flushing changes nothing), from
+// the PTX instruction rcp.approx.ftz.f32 (error <= 1 ulp).
+__device__ __forceinline__ float rcp_1to2(float d) {
+#if RMSN_FAST_EXP
+    float r;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(d));
+    return r;
+#else
+    return __fdividef(1.0f, d);
+#endif
+}
+
 // sigmoid(z) = 1 / (1 + exp(-z)) in fp32, in the stable two-sided form: with
 // e = exp(-|z|) in (0, 1] and s = 1 / (1 + e), sigmoid is s for z >= 0 and
-// e * s (= e^z / (1 + e^z)) for z < 0, so the divisor stays in (1, 2]. Uses
-// CUDA's fast intrinsics __expf (error <= 2 + floor(1.17|z|) ulp) and
-// __fdividef (<= 2 ulp on that range): a relative error of about
-// (5 + 1.17|z|) * 2^-24 on sigmoid, for every finite z.
+// e * s (= e^z / (1 + e^z)) for z < 0, so the divisor stays in [1, 2]. A
+// relative error of about (5 + 2|z|) * 2^-24 on sigmoid, for every finite z.
 __device__ __forceinline__ float sigmoidf_rn(float z) {
-    const float e = __expf(-fabsf(z));
-    const float s = __fdividef(1.0f, fadd(1.0f, e));
+    const float e = exp_neg(fabsf(z));
+    const float s = rcp_1to2(fadd(1.0f, e));
     return z >= 0.0f ? s : fmul(e, s);
 }
 
@@ -328,8 +359,8 @@ __device__ __forceinline__ float gate_value(float z) {
 }
 template <bool SIG>
 __device__ __forceinline__ void gate_eval(float z, float& q, float& dq) {
-    const float e = __expf(-fabsf(z));
-    const float s = __fdividef(1.0f, fadd(1.0f, e));
+    const float e = exp_neg(fabsf(z));
+    const float s = rcp_1to2(fadd(1.0f, e));
     const float sg = z >= 0.0f ? s : fmul(e, s);
     if (SIG) {
         q = sg;
