@@ -15,6 +15,8 @@ per step, far larger than the 129 MB L2, so no flush is needed between steps.
 
 --impl reference times the float64 CPU oracle (the only reference: the pages
 hold no runnable code) on bounded row samples of the same workload.
+--workload gated times the Qwen3-Next gated step (262144 x 128) instead, as a
+side line; it also serves as the fixed driver of the gated kernels' profile.
 """
 from __future__ import annotations
 
@@ -287,6 +289,85 @@ def run_ours(args):
     barrier()
 
 
+def run_gated(args):
+    """`--workload gated`: the Qwen3-Next gated norm step (forward, backward
+    pass 1 with dx and dz, weight-gradient pass 2) over 8192 tokens x 32 heads
+    = 262144 rows of head_v_dim 128, zero-centred weight, silu gate. Device
+    timing only (the same protocol as the default workload); this is a side
+    line and the fixed driver of the gated kernels' ncu profile."""
+    import torch
+
+    import invariant_rmsnorm_gb300 as rn
+    from invariant_rmsnorm_gb300 import synth
+
+    rank, world, local = dist_setup(args.gpus)
+    dev = torch.device("cuda", local if world > 1 else 0)
+    torch.cuda.set_device(dev)
+    rn.load()
+    g = synth.gated(dev, seed=rank)
+    T, D = g.T, g.D
+    y, dx, dz = torch.empty_like(g.x), torch.empty_like(g.x), torch.empty_like(g.x)
+    rstd, dw = torch.empty(T, device=dev), torch.empty(D, device=dev)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(ev=None):
+        if ev:
+            ev[0].record(stream)
+        rn.rmsnorm_gated_fwd(g.x, g.z, g.w, y, rstd, EPS, True, stream=stream)
+        if ev:
+            ev[1].record(stream)
+        rn.rmsnorm_gated_bwd(g.g, g.x, g.z, g.w, rstd, dx, dz, None, ws, True, stream=stream)
+        if ev:
+            ev[2].record(stream)
+        rn.rmsnorm_dgamma_reduce(ws, T, D, dw, stream=stream)
+        if ev:
+            ev[3].record(stream)
+
+    for _ in range(args.warmup):
+        step()
+    torch.cuda.synchronize()
+    sampled = list(range(0, args.steps, 16))
+    evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for k in sampled}
+    start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    sampler = ClockSampler(str(dev.index or 0))
+    barrier()
+    torch.cuda.synchronize()
+    sampler.start()
+    time.sleep(0.25)
+    start.record(stream)
+    for k in range(args.steps):
+        step(evs.get(k))
+    stop.record(stream)
+    torch.cuda.synchronize()
+    clocks = sampler.stop()
+    barrier()
+    ms_per_step = dist_max(start.elapsed_time(stop)) / args.steps
+    kms = [sum(e[i].elapsed_time(e[i + 1]) for e in evs.values()) / len(evs) for i in range(3)]
+    nbytes = T * (16 * D + 8)  # fwd 6D+4 (x, z in; y, rstd out) + bwd 10D+4 (g, x, z, rstd in; dx, dz out)
+    value = world * nbytes / (ms_per_step * 1e-3) / 1e9
+    peak, peak_kind = peaks()
+    bwd_bytes = T * (10 * D + 4)
+    if rank == 0:
+        print(json.dumps({
+            "metric": "gated RMSNorm fwd+bwd HBM GB/s at 262144 x 128, bf16", "value": round(value, 2),
+            "unit": "GB/s", "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(ms_per_step, 5), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": "gated zero-centred RMSNorm fwd+bwd (Qwen3-Next)", "T": T, "D": D,
+                       "gate": "silu", "eps": EPS, "parallelism": f"replicas x{world}",
+                       "l2": "inputs 0.54 GB per step, larger than L2; no flush"},
+            "pct_of_peak": round(100.0 * value / (world * peak), 2),
+            "kernels_ms": {"fwd": round(kms[0], 5), "bwd_pass1": round(kms[1], 5), "dgamma_pass2": round(kms[2], 5),
+                           "sampled_steps": len(evs)},
+            "roofline": {"kernel": "narrow_bwd_kernel (gated, pass 1)", "bound": "hbm",
+                         "achieved": round(bwd_bytes / (kms[1] * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
+                         "frac": round(bwd_bytes / (kms[1] * 1e-3) / 1e9 / peak, 4), "peak_kind": peak_kind,
+                         "traffic": None, "algorithmic_bytes_per_launch": bwd_bytes},
+            "gpu_launches": 3 * args.steps, "clocks": clocks}))
+    barrier()
+
+
 def run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream, steps, slab=4096):
     """Time the residual step end to end through the C ABI with pinned host
     buffers, twice: serially on one stream, and pipelined in row slabs over
@@ -516,6 +597,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed CPU-oracle sample")
+    ap.add_argument("--workload", choices=("residual", "gated"), default="residual",
+                    help="residual: the benchmark line (default); gated: the 262144 x 128 gated step, device "
+                         "timing only")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")
@@ -523,6 +607,8 @@ def main():
         ap.error("--steps must be at least 1")
     if args.impl == "reference":
         run_reference(args)
+    elif args.workload == "gated":
+        run_gated(args)
     else:
         run_ours(args)
 
