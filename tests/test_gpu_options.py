@@ -164,3 +164,49 @@ def test_f16_overflow_and_subnormal_outputs():
     assert int(sub.sum()) > 0
     check_fwd("plain", x, w, 1e-6, False, fo, name="f16 range")
     assert np.isfinite(fo["rstd"].cpu().numpy()).all()
+
+
+@pytest.mark.parametrize("workload", ["residual-f16-32768x4096", "gated-sigmoid-bf16-262144x128",
+                                      "gated-f16-262144x128"])
+def test_full_size_sampled(workload):
+    """The benchmark's and the gated workload's full sizes in the new formats and
+    gate: sampled rows against the oracle, sampled weight-gradient columns with
+    all rows, and the weight gradient bitwise equal on a repeated call."""
+    import oracle
+    from tests._helpers import assert_bf16_parity, assert_dgamma_parity, assert_rel, to_f64
+    from tests.gpu_common import chunk_rows_hint
+    if workload.startswith("residual"):
+        variant, T, D, dt, gate, zc = "residual", 32768, 4096, F16, "silu", False
+    else:
+        variant, T, D, zc = "gated", 262144, 128, True
+        dt = F16 if "f16" in workload else BF16
+        gate = "sigmoid" if "sigmoid" in workload else "silu"
+    fmt = "f16" if dt == F16 else "bf16"
+    a = _inputs(variant, T, D, 61, dt, zc, zstd=2.0)
+    fo = run_fwd(variant, a["x"], a["w"], 1e-6, zc, z=a["z"], ex=True, gate=gate)
+    bo = run_bwd(variant, a["g"], a["x"], a["w"], fo["rstd"], zc, z=a["z"], g_res=a["g_res"], ex=True, gate=gate)
+    bo2 = run_bwd(variant, a["g"], a["x"], a["w"], fo["rstd"], zc, z=a["z"], g_res=a["g_res"], ex=True, gate=gate)
+    torch.cuda.synchronize()
+    assert torch.equal(bo["dgamma"].view(torch.int32), bo2["dgamma"].view(torch.int32)), "dgamma not bitwise"
+    gen = torch.Generator().manual_seed(T + D)
+    rows = torch.cat([torch.tensor([0, T - 1]), torch.randint(0, T, (510,), generator=gen)]).to(DEV)
+    pick = lambda t: None if t is None else to_f64(t.index_select(0, rows))
+    x, g, w, r = pick(a["x"]), pick(a["g"]), to_f64(a["w"]), pick(fo["rstd"])
+    if variant == "gated":
+        z = pick(a["z"])
+        y_ref, r_ref = oracle.gated_fwd(x, z, w, 1e-6, zc, gate=gate, fmt=fmt)
+        dx_ref, dz_ref, _, diag = oracle.gated_bwd(g, x, z, w, r, zc, diagnostics=True, gate=gate, fmt=fmt)
+        assert_bf16_parity("dz", pick(bo["dz"]), dz_ref, diag["dz_pre"], diag["dz_scale"], fmt=fmt)
+    else:
+        y_ref, r_ref = oracle.rmsnorm_fwd(x, w, 1e-6, zc, fmt=fmt)
+        dx_ref, _, diag = oracle.rmsnorm_bwd(g, x, w, r, zc, g_res=pick(a["g_res"]), diagnostics=True, fmt=fmt)
+        assert torch.equal(fo["x_copy"].view(torch.int16), a["x"].view(torch.int16))
+    assert_rel("rstd", r, r_ref, 1e-5)
+    assert_bf16_parity("y", pick(fo["y"]), y_ref, fmt=fmt)
+    assert_bf16_parity("dx", pick(bo["dx"]), dx_ref, diag["dx_pre"], diag["dx_scale"], fmt=fmt)
+    cols = torch.cat([torch.tensor([0, D - 1]), torch.randint(0, D, (30,), generator=gen)]).to(DEV)
+    col = lambda t: to_f64(t.index_select(1, cols))
+    dw_ref, dw_abs = oracle.weight_grad(col(a["g"]), col(a["x"]), to_f64(fo["rstd"]),
+                                        z=None if a["z"] is None else col(a["z"]), with_abs=True, gate=gate)
+    C, n = chunk_rows_hint(T, D)
+    assert_dgamma_parity("dgamma", to_f64(bo["dgamma"].index_select(0, cols)), dw_ref, dw_abs, C, n)
