@@ -275,6 +275,25 @@ int rmsnorm_fused_add_bwd_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16*
                              int64_t T, int64_t D, int zero_centered_gamma, int dtype,
                              rmsn_stream stream);
 
+/* The backward with recomputation of the forward output, with the activation
+ * dtype (and, for the gated call, the gate) as in the *_ex calls above; y is
+ * written in the activation format, bit for bit the *_ex forward's y. */
+int rmsnorm_bwd_recompute_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                             const float* w, const float* rstd,
+                             const rmsn_act16* g_res, int64_t ldgr,
+                             rmsn_act16* dx, int64_t lddx, float* dgamma,
+                             rmsn_act16* y, int64_t ldy,
+                             void* ws, size_t ws_bytes,
+                             int64_t T, int64_t D, int zero_centered_gamma, int dtype, rmsn_stream stream);
+
+int rmsnorm_gated_bwd_recompute_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                                   const rmsn_act16* z, int64_t ldz, const float* w, const float* rstd,
+                                   rmsn_act16* dx, int64_t lddx, rmsn_act16* dz, int64_t lddz, float* dw,
+                                   rmsn_act16* y, int64_t ldy,
+                                   void* ws, size_t ws_bytes,
+                                   int64_t T, int64_t D, int zero_centered_gamma, int gate, int dtype,
+                                   rmsn_stream stream);
+
 /* Weight-gradient pass 2 on its own: sums the per-chunk partials that a backward
  * call with a NULL dgamma/dw left in ws (same T, D and workspace), in the fixed
  * order, into dgamma [D]. ws must be unchanged since that call. */

@@ -34,7 +34,7 @@ __all__ = [
     "rmsnorm_gated_bwd_recompute", "rmsnorm_gated_hf_fwd", "EXPORTED_SYMBOLS",
     "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
-    "DTYPE_CODES", "GATE_CODES",
+    "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex", "DTYPE_CODES", "GATE_CODES",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -45,6 +45,7 @@ EXPORTED_SYMBOLS = (
     "rmsnorm_gated_hf_fwd",
     "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
+    "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex",
 )
 
 # enum rmsn_dtype / enum rmsn_gate of include/rmsnorm.h
@@ -82,7 +83,8 @@ _SIGS = {
 }
 # Each *_ex call: the unsuffixed signature with `int dtype` (gated: `int gate, int dtype`) before the stream.
 for _name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
-              "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd"):
+              "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
+              "rmsnorm_bwd_recompute", "rmsnorm_gated_bwd_recompute"):
     _res, _args = _SIGS[_name]
     _extra = [_INT, _INT] if "gated" in _name else [_INT]
     _SIGS[_name + "_ex"] = (_res, _args[:-1] + _extra + [_P])
@@ -447,6 +449,39 @@ def rmsnorm_fused_add_bwd_ex(g, x, res, w, rstd, g_res, dh, dgamma, ws, zero_cen
     _check("rmsnorm_fused_add_bwd_ex", load().rmsnorm_fused_add_bwd_ex(
         _ptr(g), ldg, _ptr(x), ldx, _ptr(res), ldr, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dh), ldd,
         _ptr(dgamma), wp, wb, T, D, int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_bwd_recompute_ex(g, x, w, rstd, g_res, dx, dgamma, y, ws, zero_centered_gamma: bool = False,
+                             stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldg, ldx, lddx, ldy = _act(g, "g", T, D, dt), _act(x, "x", T, D, dt), _act(dx, "dx", T, D, dt), _act(y, "y", T, D, dt)
+    ldgr = _act(g_res, "g_res", T, D, dt) if g_res is not None else D
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dgamma is not None:
+        _f32(dgamma, "dgamma", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_bwd_recompute_ex", load().rmsnorm_bwd_recompute_ex(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(w), _ptr(rstd), _ptr(g_res), ldgr, _ptr(dx), lddx, _ptr(dgamma),
+        _ptr(y), ldy, wp, wb, T, D, int(zero_centered_gamma), _dtype_code(x), _stream(stream, x.device)))
+
+
+def rmsnorm_gated_bwd_recompute_ex(g, x, z, w, rstd, dx, dz, dw, y, ws, zero_centered_gamma: bool = True,
+                                   gate: str = "silu", stream=None):
+    T, D = x.shape
+    dt = x.dtype
+    ldg, ldx, ldz = _act(g, "g", T, D, dt), _act(x, "x", T, D, dt), _act(z, "z", T, D, dt)
+    lddx, lddz, ldy = _act(dx, "dx", T, D, dt), _act(dz, "dz", T, D, dt), _act(y, "y", T, D, dt)
+    _f32(w, "w", D)
+    _f32(rstd, "rstd", T)
+    if dw is not None:
+        _f32(dw, "dw", D)
+    wp, wb = _ws(ws)
+    _check("rmsnorm_gated_bwd_recompute_ex", load().rmsnorm_gated_bwd_recompute_ex(
+        _ptr(g), ldg, _ptr(x), ldx, _ptr(z), ldz, _ptr(w), _ptr(rstd), _ptr(dx), lddx, _ptr(dz), lddz, _ptr(dw),
+        _ptr(y), ldy, wp, wb, T, D, int(zero_centered_gamma), _gate_code(gate), _dtype_code(x),
+        _stream(stream, x.device)))
 
 
 def rmsnorm_dgamma_reduce(ws, T: int, D: int, dgamma, stream=None):

@@ -359,6 +359,52 @@ int rmsnorm_fused_add_bwd_impl(int flags, const rmsn_act16* g, int64_t ldg, cons
     return run_bwd((g_res ? kFusedAdd : kFusedAddNoGres) | flags, a, dgamma, stream);
 }
 
+int rmsnorm_bwd_recompute_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                               const float* w, const float* rstd, const rmsn_act16* g_res, int64_t ldgr,
+                               rmsn_act16* dx, int64_t lddx, float* dgamma, rmsn_act16* y, int64_t ldy, void* ws,
+                               size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.y = y; a.ldy = ldy; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd((g_res ? kResidual : kPlain) | flags, a, dgamma, stream);
+}
+
+int rmsnorm_gated_bwd_recompute_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                                     const rmsn_act16* z, int64_t ldz, const float* w, const float* rstd,
+                                     rmsn_act16* dx, int64_t lddx, rmsn_act16* dz, int64_t lddz, float* dw,
+                                     rmsn_act16* y, int64_t ldy, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                                     int zero_centered_gamma, rmsn_stream stream) {
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(z, ldz, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_act(dz, lddz, D));
+    RMSN_TRY(check_act(y, ldy, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dw) RMSN_TRY(check_vec(dw));
+    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.dz = dz; a.lddz = lddz; a.y = y; a.ldy = ldy; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    return run_bwd(kGated | flags, a, dw, stream);
+}
+
 }  // namespace
 
 // ---------------------------------------------------------------------------
@@ -539,46 +585,41 @@ int rmsnorm_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, i
                           const float* rstd, const rmsn_bf16* g_res, int64_t ldgr, rmsn_bf16* dx, int64_t lddx,
                           float* dgamma, rmsn_bf16* y, int64_t ldy, void* ws, size_t ws_bytes, int64_t T, int64_t D,
                           int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(dx, lddx, D));
-    RMSN_TRY(check_act(y, ldy, D));
-    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dgamma) RMSN_TRY(check_vec(dgamma));
-    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
-    BwdArgs a{};
-    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
-    a.dx = dx; a.lddx = lddx; a.y = y; a.ldy = ldy; a.partials = static_cast<float*>(ws);
-    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
-    return run_bwd(g_res ? kResidual : kPlain, a, dgamma, stream);
+    return rmsnorm_bwd_recompute_impl(0, g, ldg, x, ldx, w, rstd, g_res, ldgr, dx, lddx, dgamma, y, ldy, ws,
+                                      ws_bytes, T, D, zero_centered_gamma, stream);
+}
+
+int rmsnorm_bwd_recompute_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx, const float* w,
+                             const float* rstd, const rmsn_act16* g_res, int64_t ldgr, rmsn_act16* dx, int64_t lddx,
+                             float* dgamma, rmsn_act16* y, int64_t ldy, void* ws, size_t ws_bytes, int64_t T,
+                             int64_t D, int zero_centered_gamma, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    return rmsnorm_bwd_recompute_impl(f, g, ldg, x, ldx, w, rstd, g_res, ldgr, dx, lddx, dgamma, y, ldy, ws,
+                                      ws_bytes, T, D, zero_centered_gamma, stream);
 }
 
 int rmsnorm_gated_bwd_recompute(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
-                                const rmsn_bf16* z,
-                                int64_t ldz, const float* w, const float* rstd, rmsn_bf16* dx, int64_t lddx,
-                                rmsn_bf16* dz, int64_t lddz, float* dw, rmsn_bf16* y, int64_t ldy, void* ws,
-                                size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
-    RMSN_TRY(check_shape(T, D));
-    if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(z, ldz, D));
-    RMSN_TRY(check_act(dx, lddx, D));
-    RMSN_TRY(check_act(dz, lddz, D));
-    RMSN_TRY(check_act(y, ldy, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dw) RMSN_TRY(check_vec(dw));
-    RMSN_TRY(check_ws(ws, ws_bytes, T, D));
-    BwdArgs a{};
-    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.z = z; a.ldz = ldz; a.w = w; a.rstd = rstd;
-    a.dx = dx; a.lddx = lddx; a.dz = dz; a.lddz = lddz; a.y = y; a.ldy = ldy; a.partials = static_cast<float*>(ws);
-    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
-    return run_bwd(kGated, a, dw, stream);
+                                const rmsn_bf16* z, int64_t ldz, const float* w, const float* rstd, rmsn_bf16* dx,
+                                int64_t lddx, rmsn_bf16* dz, int64_t lddz, float* dw, rmsn_bf16* y, int64_t ldy,
+                                void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma,
+                                rmsn_stream stream) {
+    return rmsnorm_gated_bwd_recompute_impl(0, g, ldg, x, ldx, z, ldz, w, rstd, dx, lddx, dz, lddz, dw, y, ldy, ws,
+                                            ws_bytes, T, D, zero_centered_gamma, stream);
+}
+
+int rmsnorm_gated_bwd_recompute_ex(const rmsn_act16* g, int64_t ldg, const rmsn_act16* x, int64_t ldx,
+                                   const rmsn_act16* z, int64_t ldz, const float* w, const float* rstd,
+                                   rmsn_act16* dx, int64_t lddx, rmsn_act16* dz, int64_t lddz, float* dw,
+                                   rmsn_act16* y, int64_t ldy, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                                   int zero_centered_gamma, int gate, int dtype, rmsn_stream stream) {
+    int f = 0;
+    RMSN_TRY(dtype_flags(dtype, &f));
+    int fg = 0;
+    RMSN_TRY(gate_flags(gate, &fg));
+    f |= fg;
+    return rmsnorm_gated_bwd_recompute_impl(f, g, ldg, x, ldx, z, ldz, w, rstd, dx, lddx, dz, lddz, dw, y, ldy, ws,
+                                            ws_bytes, T, D, zero_centered_gamma, stream);
 }
 
 int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D, float* dgamma,

@@ -52,3 +52,35 @@ def test_gated_bwd_recompute_matches_forward_and_backward(D, T):
     assert torch.equal(_bits(y), _bits(fo["y"]))
     assert torch.equal(_bits(dx), _bits(ref["dx"])) and torch.equal(_bits(dz), _bits(ref["dz"]))
     assert torch.equal(dw.view(torch.int32), ref["dgamma"].view(torch.int32))
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("gate", ["silu", "sigmoid"])
+@pytest.mark.parametrize("D,T", [(128, 1000), (4096, 97)])
+def test_recompute_ex_matches_forward_and_backward(D, T, gate, dtype):
+    """The *_ex recompute calls, in both activation formats and both gates:
+    y bit for bit the *_ex forward's, dx / dz / weight gradient bit for bit the
+    *_ex backward's."""
+    x, z, g, gr = (synth.normal16((T, D), D + s, DEV, dtype=dtype) for s in (10, 11, 12, 13))
+    w = synth.gamma_f32(D, D + 14, DEV, mean=0.0, std=0.1)
+    # gated
+    fo = run_fwd("gated", x, w, 1e-6, True, z=z, ex=True, gate=gate)
+    ref = run_bwd("gated", g, x, w, fo["rstd"], True, z=z, ex=True, gate=gate)
+    dx, dz, dw = torch.empty_like(x), torch.empty_like(x), torch.empty(D, device=DEV)
+    y = empty_act(T, D, D + 8, dtype=dtype)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=DEV)
+    rn.rmsnorm_gated_bwd_recompute_ex(g, x, z, w, fo["rstd"], dx, dz, dw, y, ws, True, gate=gate)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y), _bits(fo["y"]))
+    assert torch.equal(_bits(dx), _bits(ref["dx"])) and torch.equal(_bits(dz), _bits(ref["dz"]))
+    assert torch.equal(dw.view(torch.int32), ref["dgamma"].view(torch.int32))
+    # plain / residual gradient
+    fo = run_fwd("plain", x, w, 1e-6, False, ex=True)
+    ref = run_bwd("residual", g, x, w, fo["rstd"], False, g_res=gr, ex=True)
+    dx, dg = torch.empty_like(x), torch.empty(D, device=DEV)
+    y = empty_act(T, D, D + 8, dtype=dtype)
+    rn.rmsnorm_bwd_recompute_ex(g, x, w, fo["rstd"], gr, dx, dg, y, ws, False)
+    torch.cuda.synchronize()
+    assert torch.equal(_bits(y), _bits(fo["y"]))
+    assert torch.equal(_bits(dx), _bits(ref["dx"]))
+    assert torch.equal(dg.view(torch.int32), ref["dgamma"].view(torch.int32))
