@@ -71,8 +71,21 @@
 #define RMSN_BWD_LEAN 1   // backward recomputes products after the reduction (fewer registers)
 #endif
 #ifndef RMSN_BWD_MINB
-#define RMSN_BWD_MINB 2   // backward CTAs that must fit on one SM (register budget)
+#define RMSN_BWD_MINB 2   // backward CTAs that must fit on one SM (register budget), VPT 2
 #endif
+#ifndef RMSN_BWD_MINB_V1
+#define RMSN_BWD_MINB_V1 3  // the same for VPT 1 (3 CTAs of 72 registers)
+#endif
+#ifndef RMSN_BWD_HOLD_WIDE
+#define RMSN_BWD_HOLD_WIDE 1  // VPT 4 at 512 threads: re-read staged operands after the reduction
+#endif
+#ifndef RMSN_BWD_WL1_WIDE
+#define RMSN_BWD_WL1_WIDE 1  // VPT 4 at 512 threads: weights from L1 where used
+#endif
+#ifndef RMSN_WIDE_BWD_CTAS_PER_SM_V1
+#define RMSN_WIDE_BWD_CTAS_PER_SM_V1 3
+#endif
+
 
 namespace rmsn {
 
@@ -80,6 +93,14 @@ namespace rmsn {
 // registers (a 9-warp CTA puts 3 warps on one scheduler: <= 168 registers per
 // thread) or shared memory.
 template <int VPT> __host__ __device__ constexpr int fwd_rows() { return VPT >= 4 ? 1 : RMSN_FWD_ROWS; }
+// Backward CTAs per SM that the register budget must allow, and the cap on
+// resident CTAs: 3 at VPT 1 (72 registers), 2 at VPT 2 (96), 1 beyond.
+template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_min_blocks() {
+    return (MAXT > 256 || VPT > 2) ? 1 : (VPT == 1 ? RMSN_BWD_MINB_V1 : RMSN_BWD_MINB);
+}
+template <int VPT> __host__ __device__ constexpr int bwd_ctas_per_sm() {
+    return VPT == 1 ? RMSN_WIDE_BWD_CTAS_PER_SM_V1 : RMSN_WIDE_BWD_CTAS_PER_SM;
+}
 template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_rows() {
     return (VPT == 1 && MAXT <= 256) ? RMSN_BWD_ROWS : 1;
 }
@@ -123,6 +144,20 @@ __device__ __forceinline__ void load_weights(const float* w, int zc, int NV, int
 #pragma unroll
             for (int e = 0; e < 8; ++e) we[k][e] = 0.0f;
         }
+    }
+}
+
+// Effective weights of vector v (8 values), read through the non-coherent
+// cache path where they are used (volatile: not hoisted into registers).
+__device__ __forceinline__ void weights8(const float* w, int zc, int v, float (&o)[8]) {
+    const float* p = w + 8 * v;
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(o[0]), "=f"(o[1]), "=f"(o[2]), "=f"(o[3]) : "l"(p));
+    asm volatile("ld.global.nc.v4.f32 {%0, %1, %2, %3}, [%4];"
+                 : "=f"(o[4]), "=f"(o[5]), "=f"(o[6]), "=f"(o[7]) : "l"(p + 4));
+    if (zc) {
+#pragma unroll
+        for (int e = 0; e < 8; ++e) o[e] = fadd(o[e], 1.0f);
     }
 }
 
@@ -372,7 +407,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
 // g*silu(z) for g) are computed once before it and kept in registers.
 // ---------------------------------------------------------------------------
 template <int VPT, int MODE, int MAXT>
-__global__ void __launch_bounds__(MAXT + 32, ((MAXT <= 256 && VPT <= 2) ? RMSN_BWD_MINB : 1))
+__global__ void __launch_bounds__(MAXT + 32, bwd_min_blocks<VPT, MAXT>())
 wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr int M = base_mode(MODE);
     constexpr bool F16 = is_f16(MODE);
@@ -382,6 +417,15 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr int R = bwd_rows<VPT, MAXT>();
     constexpr int NWMAX = MAXT / 32;
     static_assert(C % R == 0, "rows per iteration must divide the chunk");
+    // Register diet of the widest rows (VPT 4 on 512 threads, D > 8192, where
+    // the launch allows about 96 registers): HOLD re-reads the staged operands
+    // after the row reduction instead of keeping them packed in registers (the
+    // stage is released at the end of the iteration); WL1 reads the weights
+    // from L1 where they are used instead of keeping them in registers.
+    // Measured at D=16384: 783 -> 667 us per 32768 rows; at 256 threads
+    // (D <= 8192) both cost more than they save.
+    constexpr bool HOLD = VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE;
+    constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -449,7 +493,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     }
 
     float we[VPT][8];
-    load_weights<VPT>(a.w, a.zc, NV, nt, tid, we);
+    if (!WL1) load_weights<VPT>(a.w, a.zc, NV, nt, tid, we);
     float acc[VPT][8];
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
@@ -489,9 +533,13 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                 }
             }
         }
-        // The stage is in registers: hand it back to the producer.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        // The stage is in registers: hand it back to the producer (HOLD: after
+        // the row is done, since the operands are read again).
+        const int s_used = s;
+        if (!HOLD) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s]);
+        }
         if (++s == S) {
             s = 0;
             ph ^= 1u;
@@ -504,7 +552,11 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     if (j * nt + tid < NV) {
-                        float gf[8];
+                        float gf[8], wj[8];
+                        if (WL1) weights8(a.w, a.zc, j * nt + tid, wj);
+                        else
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) wj[e] = we[j][e];
                         unpack_act<F16>(gv[r][j], gf);
                         norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);  // x, or h = x + res
                         if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
@@ -517,7 +569,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         }
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
-                            gw[r][j][e] = fmul(gf[e], we[j][e]);
+                            gw[r][j][e] = fmul(gf[e], wj[e]);
                             if (!RMSN_BWD_LEAN) gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
                             sp[r] = fadd(sp[r], fmul(gw[r][j][e], xs[r][j][e]));
                         }
@@ -542,6 +594,18 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                 for (int j = 0; j < VPT; ++j) {
                     const int v = j * nt + tid;
                     if (v < NV) {
+                        float wj[8];
+                        if (WL1) weights8(a.w, a.zc, v, wj);
+                        else
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) wj[e] = we[j][e];
+                        if (HOLD) {  // the operands again, from the stage still held
+                            const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_bytes;
+                            gv[r][j] = ld_shared_v4(src + 16 * v);
+                            xv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
+                            if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_bytes + 16 * v);
+                            if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
+                        }
                         if (RMSN_BWD_LEAN) {
                             // Recompute the phase-1 products from the packed row (same bits).
                             float gf[8];
@@ -554,7 +618,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                     g0[r][j][e] = gf[e];
                                     gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));
                                 }
-                                gw[r][j][e] = fmul(gf[e], we[j][e]);
+                                gw[r][j][e] = fmul(gf[e], wj[e]);
                                 gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
                             }
                         }
@@ -575,7 +639,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             for (int e = 0; e < 8; ++e) {
                                 float q, dq;
                                 gate_eval<SIG>(tz[r][j][e], q, dq);
-                                const float u = fmul(fmul(xs[r][j][e], r1), we[j][e]);
+                                const float u = fmul(fmul(xs[r][j][e], r1), wj[e]);
                                 dzv[e] = fmul(fmul(g0[r][j][e], u), dq);
                                 yv[e] = fmul(u, q);
                             }
@@ -586,12 +650,16 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             // same bits as the forward's y.
                             float yv[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), we[j][e]);
+                            for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), wj[e]);
                             st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
                         }
                     }
                 }
             }
+        }
+        if (HOLD) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&empty[s_used]);
         }
         // End of a chunk: write its partial row and restart the accumulators.
         const int k_last = i * R + nvalid - 1;
@@ -661,7 +729,7 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT>);
     cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), RMSN_WIDE_BWD_CTAS_PER_SM);
+    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT>());
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nchunks = (a.T + kWideChunkRows - 1) / kWideChunkRows;
     const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
