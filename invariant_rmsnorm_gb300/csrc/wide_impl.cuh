@@ -76,6 +76,9 @@
 #ifndef RMSN_BWD_MINB_V1
 #define RMSN_BWD_MINB_V1 3  // the same for VPT 1 (3 CTAs of 72 registers)
 #endif
+#ifndef RMSN_BWD_V4_224
+#define RMSN_BWD_V4_224 1  // VPT 4 rows of at most 224 threads: a 224-thread kernel, 2 CTAs per SM
+#endif
 #ifndef RMSN_BWD_HOLD_WIDE
 #define RMSN_BWD_HOLD_WIDE 1  // VPT 4 at 512 threads: re-read staged operands after the reduction
 #endif
@@ -94,12 +97,13 @@ namespace rmsn {
 // thread) or shared memory.
 template <int VPT> __host__ __device__ constexpr int fwd_rows() { return VPT >= 4 ? 1 : RMSN_FWD_ROWS; }
 // Backward CTAs per SM that the register budget must allow, and the cap on
-// resident CTAs: 3 at VPT 1 (72 registers), 2 at VPT 2 (96), 1 beyond.
+// resident CTAs: 3 at VPT 1 (72 registers), 2 at VPT 2 (96), 2 for VPT 4 rows
+// of at most 224 threads (128 registers: 4096 < D <= 7168), 1 beyond.
 template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_min_blocks() {
-    return (MAXT > 256 || VPT > 2) ? 1 : (VPT == 1 ? RMSN_BWD_MINB_V1 : RMSN_BWD_MINB);
+    return MAXT == 224 ? 2 : ((MAXT > 256 || VPT > 2) ? 1 : (VPT == 1 ? RMSN_BWD_MINB_V1 : RMSN_BWD_MINB));
 }
-template <int VPT> __host__ __device__ constexpr int bwd_ctas_per_sm() {
-    return VPT == 1 ? RMSN_WIDE_BWD_CTAS_PER_SM_V1 : RMSN_WIDE_BWD_CTAS_PER_SM;
+template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_ctas_per_sm() {
+    return MAXT == 224 ? 2 : (VPT == 1 ? RMSN_WIDE_BWD_CTAS_PER_SM_V1 : RMSN_WIDE_BWD_CTAS_PER_SM);
 }
 template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_rows() {
     return (VPT == 1 && MAXT <= 256) ? RMSN_BWD_ROWS : 1;
@@ -729,7 +733,7 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT>);
     cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT>());
+    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT>());
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nchunks = (a.T + kWideChunkRows - 1) / kWideChunkRows;
     const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
@@ -753,7 +757,10 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     switch (c.bwd_vpt) {
         case 1: return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
         case 2: return big ? bwd_t<2, MODE, 512>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
-        case 4: return big ? bwd_t<4, MODE, 512>(a, c, st) : bwd_t<4, MODE, 256>(a, c, st);
+        case 4:
+            if (big) return bwd_t<4, MODE, 512>(a, c, st);
+            if (RMSN_BWD_V4_224 && c.bwd_threads <= 224) return bwd_t<4, MODE, 224>(a, c, st);
+            return bwd_t<4, MODE, 256>(a, c, st);
         default: return cudaErrorInvalidValue;
     }
 }
