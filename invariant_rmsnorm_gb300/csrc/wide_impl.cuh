@@ -97,13 +97,20 @@ namespace rmsn {
 // thread) or shared memory.
 template <int VPT> __host__ __device__ constexpr int fwd_rows() { return VPT >= 4 ? 1 : RMSN_FWD_ROWS; }
 // Backward CTAs per SM that the register budget must allow, and the cap on
-// resident CTAs: 3 at VPT 1 (72 registers), 2 at VPT 2 (96), 2 for VPT 4 rows
-// of at most 224 threads (128 registers: 4096 < D <= 7168), 1 beyond.
-template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_min_blocks() {
-    return MAXT == 224 ? 2 : ((MAXT > 256 || VPT > 2) ? 1 : (VPT == 1 ? RMSN_BWD_MINB_V1 : RMSN_BWD_MINB));
+// resident CTAs: 3 at VPT 1 (72 registers) for the modes that fit there
+// without spilling (not the gated or the fused-add-with-gradient backward), 2
+// at VPT 1 otherwise and at VPT 2 (96), 2 for VPT 4 rows of at most 224
+// threads (128 registers: 4096 < D <= 7168), 1 beyond.
+template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_min_blocks() {
+    return MAXT == 224 ? 2
+           : (MAXT > 256 || VPT > 2) ? 1
+           : (VPT == 1 && !is_gated(MODE) && base_mode(MODE) != kFusedAdd) ? RMSN_BWD_MINB_V1
+                                                                           : RMSN_BWD_MINB;
 }
-template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_ctas_per_sm() {
-    return MAXT == 224 ? 2 : (VPT == 1 ? RMSN_WIDE_BWD_CTAS_PER_SM_V1 : RMSN_WIDE_BWD_CTAS_PER_SM);
+template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_ctas_per_sm() {
+    return MAXT == 224 ? 2
+           : (VPT == 1 && !is_gated(MODE) && base_mode(MODE) != kFusedAdd) ? RMSN_WIDE_BWD_CTAS_PER_SM_V1
+                                                                           : RMSN_WIDE_BWD_CTAS_PER_SM;
 }
 template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_rows() {
     return (VPT == 1 && MAXT <= 256) ? RMSN_BWD_ROWS : 1;
@@ -411,7 +418,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
 // g*silu(z) for g) are computed once before it and kept in registers.
 // ---------------------------------------------------------------------------
 template <int VPT, int MODE, int MAXT>
-__global__ void __launch_bounds__(MAXT + 32, bwd_min_blocks<VPT, MAXT>())
+__global__ void __launch_bounds__(MAXT + 32, bwd_min_blocks<VPT, MAXT, MODE>())
 wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr int M = base_mode(MODE);
     constexpr bool F16 = is_f16(MODE);
@@ -733,7 +740,7 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT>);
     cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT>());
+    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT, MODE>());
     if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nchunks = (a.T + kWideChunkRows - 1) / kWideChunkRows;
     const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
