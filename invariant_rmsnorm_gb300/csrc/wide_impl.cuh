@@ -45,7 +45,9 @@
 #include "kernels.h"
 
 // Launch shapes, chosen by measurement on GB300 (T=32768, D=4096): the
-// forward runs 3 CTAs of 96 KB rings per SM; the backward 2 CTAs of 64 KB.
+// forward gets a 96 KB ring budget and as many CTAs per SM as fit (up to 3;
+// 2 at D=4096); the backward 2 CTAs of 64 KB rings (per-width exceptions at
+// bwd_min_blocks below).
 #ifndef RMSN_WIDE_FWD_SMEM
 #define RMSN_WIDE_FWD_SMEM (96 * 1024)   // target ring bytes per CTA (forward)
 #endif
@@ -700,11 +702,16 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
 
 constexpr int kMaxSmemPerCta = 227 * 1024;
 
+// Ring stages for a budget: at least 2, fewer than the budget allows only if
+// the shared memory of a CTA cannot hold them, and 1 when even two stages do
+// not fit (the four operands of a fused-add backward row beyond D = 14520).
+// With one stage the consumers still hand it back as soon as it is in
+// registers, so the next row's copy overlaps the row's arithmetic.
 inline int stages_for(size_t budget, size_t stage_bytes, size_t per_stage_extra, size_t fixed) {
     size_t s = budget / stage_bytes;
     if (s > RMSN_MAX_STAGES) s = RMSN_MAX_STAGES;
-    while (s > 2 && s * (stage_bytes + per_stage_extra) + fixed > static_cast<size_t>(kMaxSmemPerCta)) --s;
     if (s < 2) s = 2;
+    while (s > 1 && s * (stage_bytes + per_stage_extra) + fixed > static_cast<size_t>(kMaxSmemPerCta)) --s;
     return static_cast<int>(s);
 }
 

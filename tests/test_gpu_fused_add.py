@@ -35,7 +35,8 @@ def _case(T, D, seed, zc=False, with_gres=True, ld_in=None, ld_out=None, name=""
 
 
 @pytest.mark.parametrize("with_gres", [True, False])
-@pytest.mark.parametrize("D,T", [(D, T) for D in (8, 128, 256, 264, 2048, 4096, 7168) for T in (1, 70, 333)])
+@pytest.mark.parametrize("D,T", [(D, T) for D in (8, 128, 256, 264, 2048, 4096, 7168) for T in (1, 70, 333)]
+                         + [(14528, 40), (16384, 33)])
 def test_fused_add_shapes(D, T, with_gres):
     _case(T, D, seed=D + 3 * T, with_gres=with_gres, name=f"fused T={T} D={D}")
 

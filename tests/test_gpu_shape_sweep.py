@@ -1,0 +1,63 @@
+"""Seeded sweep over row widths and batch sizes.
+
+The kernels pick their launch shape from D alone (narrow lane groups of 1 to
+32 lanes, wide rows of 1, 2 or 4 vectors per thread on 224, 256 or 512
+threads) and from the mode (which fixes registers and CTAs per SM). This
+sweep draws widths across the whole supported range, 8 to 16384 in steps of
+8, with ragged batch sizes, and checks every variant in both activation
+formats against the oracle: outputs within one ulp (or the cancellation
+bound), rstd within 1e-5 relative, the weight gradient within 1e-4 relative
+(or the fixed tree's bound). Widths at each launch-shape boundary are
+always included.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_rmsnorm_gb300 import synth
+from tests.gpu_common import DEV, check_bwd, check_fwd, run_bwd, run_fwd
+
+pytestmark = pytest.mark.gpu
+
+# Boundaries of the launch shapes (in elements): narrow groups (<= 256), wide
+# VPT 1 (<= 2048 at 256 threads), VPT 2 (<= 4096), VPT 4 on <= 224 threads
+# (<= 7168), on 256 (<= 8192), on 512 threads (> 8192).
+BOUNDARY_D = [8, 16, 136, 256, 264, 2048, 2056, 4096, 4104, 7168, 7176, 8192, 8200, 16384]
+
+
+def _draws(n, seed=2024):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(n):
+        D = int(rng.integers(1, 2049)) * 8
+        T = int(rng.integers(1, 200)) if D <= 4096 else int(rng.integers(1, 60))
+        out.append((D, T))
+    return out
+
+
+CASES = [(D, 37 if D <= 4096 else 19) for D in BOUNDARY_D] + _draws(24)
+VARIANTS = ["plain", "residual", "gated", "fused"]
+
+
+@pytest.mark.parametrize("D,T", CASES)
+def test_shape_sweep(D, T):
+    rng = np.random.default_rng(D * 7919 + T)
+    variant = VARIANTS[int(rng.integers(0, 4))]
+    dtype = torch.float16 if rng.integers(0, 2) else torch.bfloat16
+    gate = "sigmoid" if rng.integers(0, 2) else "silu"
+    zc = bool(rng.integers(0, 2))
+    seed = int(rng.integers(0, 1 << 20))
+    x = synth.normal16((T, D), seed, DEV, dtype=dtype)
+    g = synth.normal16((T, D), seed + 1, DEV, dtype=dtype)
+    w = synth.gamma_f32(D, seed + 2, DEV, mean=0.0 if zc else 1.0, std=0.1)
+    z = synth.normal16((T, D), seed + 3, DEV, std=2.0, dtype=dtype) if variant == "gated" else None
+    gr = synth.normal16((T, D), seed + 4, DEV, dtype=dtype) if variant in ("residual", "fused") else None
+    res = synth.normal16((T, D), seed + 5, DEV, std=4.0, dtype=dtype) if variant == "fused" else None
+    name = f"{variant} {dtype} {gate} zc={zc} T={T} D={D}"
+    fo = run_fwd(variant, x, w, 1e-6, zc, z=z, res=res, ex=True, gate=gate)
+    bo = run_bwd(variant, g, x, w, fo["rstd"], zc, z=z, g_res=gr, res=res, ex=True, gate=gate)
+    torch.cuda.synchronize()
+    check_fwd(variant, x, w, 1e-6, zc, fo, z=z, res=res, gate=gate, name=name)
+    check_bwd(variant, g, x, w, fo["rstd"], zc, bo, z=z, g_res=gr, res=res, gate=gate, name=name)
