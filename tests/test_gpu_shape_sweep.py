@@ -61,3 +61,37 @@ def test_shape_sweep(D, T):
     torch.cuda.synchronize()
     check_fwd(variant, x, w, 1e-6, zc, fo, z=z, res=res, gate=gate, name=name)
     check_bwd(variant, g, x, w, fo["rstd"], zc, bo, z=z, g_res=gr, res=res, gate=gate, name=name)
+
+
+@pytest.mark.parametrize("D,T", _draws(12, seed=77) + [(7168, 21), (8192, 13), (16384, 9)])
+def test_shape_sweep_strided_recompute(D, T):
+    """Random widths with padded row strides on every input and output, through
+    the recompute backward: its y is the forward's bit for bit, its dx and
+    weight gradient the plain backward's, and the pad columns stay untouched."""
+    import invariant_rmsnorm_gb300 as rn
+    from tests.gpu_common import empty_act
+    rng = np.random.default_rng(D + 31 * T)
+    dtype = torch.float16 if rng.integers(0, 2) else torch.bfloat16
+    zc = bool(rng.integers(0, 2))
+    ld_in, ld_out = D + 8 * int(rng.integers(1, 9)), D + 8 * int(rng.integers(1, 9))
+    x = synth.strided(synth.normal16((T, D), D, DEV, dtype=dtype), ld_in)
+    g = synth.strided(synth.normal16((T, D), D + 1, DEV, dtype=dtype), ld_in + 8)
+    gr = synth.strided(synth.normal16((T, D), D + 2, DEV, dtype=dtype), ld_in + 16)
+    w = synth.gamma_f32(D, D + 3, DEV, mean=0.0 if zc else 1.0, std=0.1)
+    fo = run_fwd("plain", x, w, 1e-6, zc, ld_out=ld_out, ex=True)
+    ref = run_bwd("residual", g, x, w, fo["rstd"], zc, g_res=gr, ld_out=ld_out, ex=True)
+    y = empty_act(T, D, ld_out, fill=5.0, dtype=dtype)
+    dx = empty_act(T, D, ld_out, fill=5.0, dtype=dtype)
+    dg = torch.empty(D, device=DEV)
+    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=DEV)
+    rn.rmsnorm_bwd_recompute_ex(g, x, w, fo["rstd"], gr, dx, dg, y, ws, zc)
+    torch.cuda.synchronize()
+    bits = lambda t: t.contiguous().view(torch.int16)
+    assert torch.equal(bits(y), bits(fo["y"])) and torch.equal(bits(dx), bits(ref["dx"]))
+    assert torch.equal(dg.view(torch.int32), ref["dgamma"].view(torch.int32))
+    for t in (y, dx):  # the pad columns of the padded outputs are untouched
+        full = t.as_strided((T, ld_out), (ld_out, 1))
+        assert torch.all(full[:, D:].float() == 5.0)
+    name = f"strided {dtype} zc={zc} T={T} D={D}"
+    check_fwd("plain", x, w, 1e-6, zc, fo, name=name)
+    check_bwd("residual", g, x, w, fo["rstd"], zc, ref, g_res=gr, name=name)
