@@ -94,10 +94,21 @@
 
 namespace rmsn {
 
-// Rows per iteration. Larger rows need no batching, and R > 1 would overflow
-// registers (a 9-warp CTA puts 3 warps on one scheduler: <= 168 registers per
-// thread) or shared memory.
-template <int VPT> __host__ __device__ constexpr int fwd_rows() { return VPT >= 4 ? 1 : RMSN_FWD_ROWS; }
+// Rows per iteration: 4 (forward) or 2 (backward at VPT 1) for narrow wide
+// rows; at VPT 4 the forward takes 2 rows when it streams one operand
+// (plain, residual; 32768 x 16384: 498 -> 338 us) and 1 otherwise, since a
+// second row of two operands overflows registers (a 9-warp CTA puts 3 warps
+// on one scheduler: <= 168 registers per thread) or shared memory.
+#ifndef RMSN_FWD_ROWS_V4
+#define RMSN_FWD_ROWS_V4 2  // VPT 4 rows on 512 threads (D > 8192), one streamed operand: 2 rows per iteration
+#endif
+#ifndef RMSN_FWD_ROWS_V4_256
+#define RMSN_FWD_ROWS_V4_256 2  // VPT 4 rows on up to 256 threads, one streamed operand
+#endif
+template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int fwd_rows() {
+    return VPT < 4 ? RMSN_FWD_ROWS
+                   : (fwd_inputs(MODE) > 1 ? 1 : (MAXT > 256 ? RMSN_FWD_ROWS_V4 : RMSN_FWD_ROWS_V4_256));
+}
 // Backward CTAs per SM that the register budget must allow, and the cap on
 // resident CTAs: 3 at VPT 1 (72 registers) for the modes that fit there
 // without spilling (not the gated or the fused-add-with-gradient backward), 2
@@ -259,7 +270,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
     constexpr bool SIG = is_sigmoid_gate(MODE);
     static_assert(!(M == kGatedHF && F16), "the HF-convention witness is a bf16 forward");
     constexpr int NIN = fwd_inputs(MODE);
-    constexpr int R = fwd_rows<VPT>();
+    constexpr int R = fwd_rows<VPT, MAXT, MODE>();
     constexpr int NWMAX = MAXT / 32;
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
@@ -718,7 +729,7 @@ inline int stages_for(size_t budget, size_t stage_bytes, size_t per_stage_extra,
 template <int VPT, int MODE, int MAXT>
 cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
     constexpr int NIN = fwd_inputs(MODE);
-    constexpr int R = fwd_rows<VPT>();
+    constexpr int R = fwd_rows<VPT, MAXT, MODE>();
     const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
     const size_t fixed = 2 * R * 32 * 4;
     const int S = stages_for(RMSN_WIDE_FWD_SMEM, stage, 16, fixed);
