@@ -22,6 +22,9 @@ namespace rmsn {
 #ifndef RMSN_BWD_NTMAX
 #define RMSN_BWD_NTMAX 256
 #endif
+#ifndef RMSN_BWD_NT128_UPTO
+#define RMSN_BWD_NT128_UPTO 256  // plain backward rows of at most this many 16-byte vectors (D <= 2048): <= 128 threads
+#endif
 
 // Threads and 16-byte vectors per thread for one row of NV vectors: at most
 // `ntmax` threads (512 beyond 1024 vectors), VPT in {1, 2, 4}, threads rounded
@@ -188,7 +191,13 @@ int run_fwd(int m, FwdArgs a, cudaStream_t s) {
 
 int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     a.inv_d_pow2 = inv_pow2(a.D);
-    const RowCfg c = row_cfg(a.D);
+    RowCfg c = row_cfg(a.D);
+    // The plain backward of rows up to 2048 values runs them on at most 128
+    // threads, two vectors each (a fixed function of D for this mode; measured
+    // 131072 x 2048: 291 -> 282 us). The modes streaming more operands per row
+    // measured slower that way and keep the shared shape.
+    if (!c.narrow && base_mode(m) == kPlain && a.D / 8 <= RMSN_BWD_NT128_UPTO)
+        wide_shape(a.D / 8, 128, &c.bwd_threads, &c.bwd_vpt);
     cudaError_t e;
     if (is_f16(m)) e = c.narrow ? launch_narrow_bwd_f16(m, a, c, s) : launch_wide_bwd_f16(m, a, c, s);
     else e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);

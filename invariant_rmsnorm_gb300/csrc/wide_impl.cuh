@@ -115,13 +115,13 @@ template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int fwd_row
 // at VPT 1 otherwise and at VPT 2 (96), 2 for VPT 4 rows of at most 224
 // threads (128 registers: 4096 < D <= 7168), 1 beyond.
 template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_min_blocks() {
-    return MAXT == 224 ? 2
+    return MAXT == 128 ? 4 : MAXT == 224 ? 2
            : (MAXT > 256 || VPT > 2) ? 1
            : (VPT == 1 && !is_gated(MODE) && base_mode(MODE) != kFusedAdd) ? RMSN_BWD_MINB_V1
                                                                            : RMSN_BWD_MINB;
 }
 template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_ctas_per_sm() {
-    return MAXT == 224 ? 2
+    return MAXT == 128 ? 4 : MAXT == 224 ? 2
            : (VPT == 1 && !is_gated(MODE) && base_mode(MODE) != kFusedAdd) ? RMSN_WIDE_BWD_CTAS_PER_SM_V1
                                                                            : RMSN_WIDE_BWD_CTAS_PER_SM;
 }
@@ -781,7 +781,10 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const bool big = c.bwd_threads > 256;
     switch (c.bwd_vpt) {
         case 1: return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
-        case 2: return big ? bwd_t<2, MODE, 512>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
+        case 2:
+            if (big) return bwd_t<2, MODE, 512>(a, c, st);
+            if (c.bwd_threads <= 128) return bwd_t<2, MODE, 128>(a, c, st);  // rows of 2 vectors a thread on <= 128 threads
+            return bwd_t<2, MODE, 256>(a, c, st);
         case 4:
             if (big) return bwd_t<4, MODE, 512>(a, c, st);
             if (RMSN_BWD_V4_224 && c.bwd_threads <= 224) return bwd_t<4, MODE, 224>(a, c, st);
