@@ -59,10 +59,16 @@ def peaks():
     return 6800.0, "fallback"
 
 
+# The files that build backward pass 1 at D=4096 and choose its launch shape;
+# host-only conveniences of the library (noalloc.cu, host_step.cu) and the
+# other activation format's instantiations are not among them.
+KERNEL_SOURCES = ("api.cu", "common.cuh", "kernels.h", "reduce.cu", "wide.cu", "wide_impl.cuh")
+
+
 def source_hash():
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "invariant_rmsnorm_gb300", "csrc")
-    for name in sorted(os.listdir(csrc)):
+    for name in KERNEL_SOURCES:
         with open(os.path.join(csrc, name), "rb") as f:
             h.update(name.encode() + f.read())
     return h.hexdigest()[:16]
@@ -277,7 +283,7 @@ def run_ours(args):
                              "frac": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9 / peak, 4)},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                    "how": "4096-row slabs pipelined over H2D / compute / D2H streams",
+                    "how": "rmsnorm_residual_step_host: 4096-row slabs, copies overlapped with the kernels inside the library",
                     "bitwise_equal_to_unsliced_step": e2e_same_bits,
                     "serial_value": round(e2e_serial_value, 2), "serial_ms_per_step": round(e2e_ms_serial, 4)},
             "gpu_launches": 3 * args.steps,
@@ -370,11 +376,11 @@ def run_gated(args):
 
 def run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream, steps, slab=4096):
     """Time the residual step end to end through the C ABI with pinned host
-    buffers, twice: serially on one stream, and pipelined in row slabs over
-    three streams (copies of slab k+1 in and slab k-1 out overlap the kernels
-    of slab k). Slabs are whole weight-gradient chunks, so each slab's
-    backward writes its own chunk partials and one pass 2 over all rows gives
-    the same dgamma bits as the unsliced step (checked).
+    buffers, twice: serially on one stream (copies in, the two device entry
+    points, copies out), and through rmsnorm_residual_step_host, which
+    pipelines row slabs inside the library (copies of slab k+1 in and slab k-1
+    out overlap the kernels of slab k). Its outputs are checked bitwise
+    against the serial step's.
     Returns (serial ms, pipelined ms, H2D bytes, D2H bytes, bits equal)."""
     import torch
     dev = wl.x.device
@@ -386,7 +392,6 @@ def run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream, steps, slab=4096):
     h_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
     h2d = sum(t.numel() * t.element_size() for t in h_in) + h_w.numel() * 4
     d2h = sum(t.numel() * t.element_size() for t in h_out)
-    row_ws = rn.workspace_bytes(32, D)  # bytes of one 32-row chunk's partial row
 
     def serial_step():
         for h, d in zip(h_in, d_in):
@@ -397,47 +402,14 @@ def run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream, steps, slab=4096):
         for h, d in zip(h_out, outs):
             h.copy_(d, non_blocking=True)
 
-    s_in, s_cmp, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev), torch.cuda.Stream(dev)
-    bounds = [(a, min(a + slab, T)) for a in range(0, T, slab)]
-    ev_in = [torch.cuda.Event() for _ in bounds]
-    ev_cmp = [torch.cuda.Event() for _ in bounds]
-    ev_out = [torch.cuda.Event() for _ in bounds]
-    ev_w, ev_red = torch.cuda.Event(), torch.cuda.Event()
+    # The pipelined step is one library call: rmsnorm_residual_step_host cuts
+    # the rows into slabs and overlaps each slab's copies with the kernels of
+    # its neighbours on the library's own copy streams.
+    work = torch.empty(rn.rmsnorm_residual_step_host_work_bytes(T, D, slab), dtype=torch.uint8, device=dev)
 
     def pipelined_step():
-        s_in.wait_stream(stream)
-        s_cmp.wait_stream(stream)
-        s_out.wait_stream(stream)
-        with torch.cuda.stream(s_in):
-            d_w.copy_(h_w, non_blocking=True)
-            ev_w.record(s_in)
-        for k, (a, b) in enumerate(bounds):
-            with torch.cuda.stream(s_in):
-                s_in.wait_event(ev_cmp[k])       # previous step done reading this slab
-                for h, d in zip(h_in, d_in):
-                    d[a:b].copy_(h[a:b], non_blocking=True)
-                ev_in[k].record(s_in)
-            s_cmp.wait_event(ev_in[k])
-            s_cmp.wait_event(ev_w)
-            s_cmp.wait_event(ev_out[k])          # previous step done copying this slab out
-            wsk = ws[(a // 32) * row_ws:]
-            rn.rmsnorm_residual_fwd(d_in[0][a:b], d_w, y[a:b], rstd[a:b], xc[a:b], EPS, False, stream=s_cmp)
-            rn.rmsnorm_residual_bwd(d_in[1][a:b], d_in[0][a:b], d_w, rstd[a:b], d_in[2][a:b], dx[a:b], None,
-                                    wsk, False, stream=s_cmp)
-            ev_cmp[k].record(s_cmp)
-            with torch.cuda.stream(s_out):
-                s_out.wait_event(ev_cmp[k])
-                for h, d in zip(h_out[:4], outs[:4]):
-                    h[a:b].copy_(d[a:b], non_blocking=True)
-                ev_out[k].record(s_out)
-        rn.rmsnorm_dgamma_reduce(ws, T, D, dg, stream=s_cmp)
-        ev_red.record(s_cmp)
-        with torch.cuda.stream(s_out):
-            s_out.wait_event(ev_red)
-            h_out[4].copy_(dg, non_blocking=True)
-        stream.wait_stream(s_in)
-        stream.wait_stream(s_cmp)
-        stream.wait_stream(s_out)
+        rn.rmsnorm_residual_step_host(h_in[0], h_in[1], h_in[2], h_w, h_out[0], h_out[1], h_out[3], h_out[2],
+                                      h_out[4], work, EPS, False, slab_rows=slab, stream=stream)
 
     def timed(fn):
         for _ in range(3):

@@ -323,6 +323,48 @@ int rmsnorm_bwd_noalloc(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int
                         rmsn_bf16* dx, int64_t lddx, float* dgamma,
                         int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream);
 
+/* rmsnorm_residual forward + backward on HOST buffers (no counterpart in the
+ * pages: a library convenience around [Residual]'s forward and backward). One
+ * call copies the inputs in, runs rmsnorm_residual_fwd_ex and
+ * rmsnorm_residual_bwd_ex, and copies every output back, with the copies
+ * overlapped against the kernels: the rows go in slabs, and while slab k's
+ * kernels run, slab k+1's inputs come in and slab k-1's outputs go out.
+ *   Host buffers, dense row-major (row stride D), in the activation format
+ *   `dtype` (RMSN_DTYPE_BF16 / RMSN_DTYPE_F16) unless marked fp32:
+ *     in:  x [T][D], g [T][D] (dL/dy), g_res [T][D] (dL/dx_copy; NULL = zero),
+ *          w [D] fp32
+ *     out: y [T][D], x_copy [T][D], rstd [T] fp32, dx [T][D], dgamma [D] fp32
+ *   Results are bitwise those of rmsnorm_residual_fwd_ex followed by
+ *   rmsnorm_residual_bwd_ex on device copies of the same inputs.
+ *   - The host buffers are read and written asynchronously: the caller must
+ *     not touch them until the work on `stream` has completed. Page-locked
+ *     (pinned) host memory gives the overlap; pageable memory is accepted but
+ *     the copies then run in step with the calling thread.
+ *   - work: a DEVICE buffer, 256-byte aligned, of at least
+ *     rmsnorm_residual_step_host_work_bytes(T, D, slab_rows) bytes, owned by the
+ *     caller. It holds three slab slots (six [slab][D] activation buffers and
+ *     a [slab] fp32 buffer each), w, dgamma and the weight-gradient partials of
+ *     all T rows. Too small or NULL: RMSN_EWORKSPACE; misaligned: RMSN_EALIGN.
+ *     Calls that overlap on the GPU must not share one work buffer.
+ *   - slab_rows: rows per slab, rounded up to the weight-gradient chunk (32
+ *     rows for D > 256) and capped at T; 0 takes the default, 4096.
+ *   - The kernels run on `stream`; the copies run on two copy streams per
+ *     device that the library creates on the first call made with that device
+ *     current (make that first call outside any stream capture) and keeps
+ *     until the process exits. The call starts after the earlier work on
+ *     `stream`, and `stream` waits for the last copy, so it is ordered like any
+ *     other work on `stream`. Calls from several host threads are serialised
+ *     while they enqueue.
+ *   - Every argument is validated before anything is enqueued. A CUDA failure
+ *     while enqueueing (RMSN_ECUDA) may leave part of the step enqueued. */
+size_t rmsnorm_residual_step_host_work_bytes(int64_t T, int64_t D, int64_t slab_rows);
+int rmsnorm_residual_step_host(const rmsn_act16* x, const rmsn_act16* g, const rmsn_act16* g_res,
+                               const float* w,
+                               rmsn_act16* y, rmsn_act16* x_copy, float* rstd,
+                               rmsn_act16* dx, float* dgamma,
+                               int64_t T, int64_t D, float eps, int zero_centered_gamma, int dtype,
+                               int64_t slab_rows, void* work, size_t work_bytes, rmsn_stream stream);
+
 /* Reads the device-side error flags of the current device (OR of all kernels'
  * flags since the last clear) into *flags; clears them if `clear` is non-zero.
  * Synchronises with the device. 0 means no kernel ever gave up on a wait. */

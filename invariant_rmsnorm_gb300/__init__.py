@@ -35,6 +35,7 @@ __all__ = [
     "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
     "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex", "DTYPE_CODES", "GATE_CODES",
+    "rmsnorm_residual_step_host", "rmsnorm_residual_step_host_work_bytes",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -46,6 +47,7 @@ EXPORTED_SYMBOLS = (
     "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
     "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex",
+    "rmsnorm_residual_step_host_work_bytes", "rmsnorm_residual_step_host",
 )
 
 # enum rmsn_dtype / enum rmsn_gate of include/rmsnorm.h
@@ -81,6 +83,8 @@ _SIGS = {
     "rmsnorm_gated_bwd_recompute": (_INT, [_P, _I64, _P, _I64, _P, _I64, _P, _P, _P, _I64, _P, _I64, _P, _P, _I64,
                                            _P, _SZ, _I64, _I64, _INT, _P]),
 }
+_SIGS["rmsnorm_residual_step_host_work_bytes"] = (_SZ, [_I64, _I64, _I64])
+_SIGS["rmsnorm_residual_step_host"] = (_INT, [_P] * 9 + [_I64, _I64, _F, _INT, _INT, _I64, _P, _SZ, _P])
 # Each *_ex call: the unsuffixed signature with `int dtype` (gated: `int gate, int dtype`) before the stream.
 for _name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
               "rmsnorm_fused_add_fwd", "rmsnorm_fused_add_bwd", "rmsnorm_gated_fwd", "rmsnorm_gated_bwd",
@@ -510,3 +514,36 @@ def rmsnorm_device_error(clear: bool = True) -> int:
     flags = ctypes.c_uint(0)
     _check("rmsnorm_device_error", load().rmsnorm_device_error(ctypes.byref(flags), int(clear)))
     return int(flags.value)
+
+
+def _host(t: torch.Tensor, name: str, shape, dtype: torch.dtype):
+    if t.dtype != dtype or t.is_cuda or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise TypeError(f"{name}: expected a contiguous host {dtype} tensor of shape {tuple(shape)}, got "
+                        f"{t.dtype} {t.device} {tuple(t.shape)}")
+
+
+def rmsnorm_residual_step_host_work_bytes(T: int, D: int, slab_rows: int = 0) -> int:
+    return int(load().rmsnorm_residual_step_host_work_bytes(int(T), int(D), int(slab_rows)))
+
+
+def rmsnorm_residual_step_host(x, g, g_res, w, y, x_copy, rstd, dx, dgamma, work, eps: float = 1e-6,
+                               zero_centered_gamma: bool = False, slab_rows: int = 0, stream=None):
+    """rmsnorm_residual forward + backward on HOST tensors (pinned for overlap):
+    one call copies the inputs in, runs both kernels and copies every output
+    back, pipelined in row slabs inside the library. ``work`` is a CUDA byte
+    buffer of ``rmsnorm_residual_step_host_work_bytes(T, D, slab_rows)`` bytes;
+    the host tensors must not be touched until ``stream`` has completed."""
+    T, D = x.shape
+    dt = x.dtype
+    for t, n in ((x, "x"), (g, "g"), (y, "y"), (x_copy, "x_copy"), (dx, "dx")):
+        _host(t, n, (T, D), dt)
+    if g_res is not None:
+        _host(g_res, "g_res", (T, D), dt)
+    _host(w, "w", (D,), torch.float32)
+    _host(dgamma, "dgamma", (D,), torch.float32)
+    _host(rstd, "rstd", (T,), torch.float32)
+    wp, wb = _ws(work)
+    _check("rmsnorm_residual_step_host", load().rmsnorm_residual_step_host(
+        _ptr(x), _ptr(g), _ptr(g_res), _ptr(w), _ptr(y), _ptr(x_copy), _ptr(rstd), _ptr(dx), _ptr(dgamma),
+        T, D, float(eps), int(zero_centered_gamma), _dtype_code(x), int(slab_rows), wp, wb,
+        _stream(stream, work.device)))

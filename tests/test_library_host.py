@@ -109,6 +109,42 @@ def test_ex_options_are_validated_on_the_host(lib):
     assert lib.rmsnorm_residual_fwd_ex(0, 0, 0, 0, 0, 0, 0, 0, 0, 128, 1e-6, 0, 1, None) == 0  # T = 0
 
 
+@pytest.mark.parametrize("T,D", [(1, 128), (100, 64), (32768, 4096), (4097, 4096), (70000, 8)])
+def test_host_step_work_query(lib, T, D):
+    """The host-buffer step's device work buffer: the weight-gradient partials
+    of all T rows, plus up to three slab slots of six activation buffers and
+    one fp32 buffer; slabs are whole chunks, capped at T; 0 = the default."""
+    q = rn.rmsnorm_residual_step_host_work_bytes
+    part = rn.rmsnorm_bwd_workspace_bytes(T, D)
+    b = q(T, D)
+    assert b == q(T, D, 4096) and b % 256 == 0
+    slab = min(4096, T)
+    slots = min(3, -(-T // 4096))
+    assert b >= part + slots * (6 * slab * D * 2 + slab * 4)
+    assert b < part + slots * (6 * (slab + 256) * D * 2 + (slab + 256) * 4) + 8 * D + 4096
+    assert q(T, D, 10 ** 9) == q(T, D, T)                 # capped at T
+    assert q(T, D, 1) <= b                                # one chunk per slab
+    assert q(0, D) == 0 and q(T, 7) == 0 and q(T, D, -1) == 0
+
+
+def test_host_step_validation_rejects_before_launch(lib):
+    """The host-buffer step checks every argument before it enqueues anything."""
+    A = 1 << 20
+    need = rn.rmsnorm_residual_step_host_work_bytes(64, 128)
+
+    def step(x=A, dt=0, T=64, D=128, eps=1e-6, slab=0, work=A * 16, wb=need, gres=A):
+        return lib.rmsnorm_residual_step_host(x, A, gres, A, A, A, A, A, A, T, D, eps, 0, dt, slab, work, wb, None)
+
+    assert step(dt=2) == -1                    # unknown activation format
+    assert step(D=7) == -3 and step(D=16392) == -3
+    assert step(eps=float("nan")) == -1 and step(eps=-1.0) == -1
+    assert step(T=-1) == -1 and step(slab=-4) == -1
+    assert step(x=0, T=0, work=0, wb=0) == 0   # empty: OK, nothing enqueued
+    assert step(x=0) == -1                     # null host input
+    assert step(work=0) == -5 and step(wb=need - 1) == -5
+    assert step(work=A * 16 + 16) == -2        # work not 256-byte aligned
+
+
 def test_package_has_no_non_cuda_path():
     """The binding refuses to run without the built library (no fallback)."""
     import importlib
