@@ -25,6 +25,9 @@ namespace rmsn {
 #ifndef RMSN_BWD_NT128_UPTO
 #define RMSN_BWD_NT128_UPTO 256  // plain backward rows of at most this many 16-byte vectors (D <= 2048): <= 128 threads
 #endif
+#ifndef RMSN_BWD_NT512_FROM
+#define RMSN_BWD_NT512_FROM 897  // backward rows of 897..1024 vectors (7168 < D <= 8192): 512 threads, 2 vectors each
+#endif
 
 // Threads and 16-byte vectors per thread for one row of NV vectors: at most
 // `ntmax` threads (512 beyond 1024 vectors), VPT in {1, 2, 4}, threads rounded
@@ -198,6 +201,13 @@ int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     // measured slower that way and keep the shared shape.
     if (!c.narrow && base_mode(m) == kPlain && a.D / 8 <= RMSN_BWD_NT128_UPTO)
         wide_shape(a.D / 8, 128, &c.bwd_threads, &c.bwd_vpt);
+    // Rows of 7168 < D <= 8192 run on 512 threads, two vectors each, rather than
+    // 256 threads with four: the four-vector kernel needs 168 registers, so a
+    // single 9-warp CTA fits on an SM, where this one keeps 16 consumer warps
+    // (measured 131072 x 8192: 1124 -> 1101 us, with the larger ring the
+    // one-CTA-per-SM backward gets).
+    if (!c.narrow && a.D / 8 >= RMSN_BWD_NT512_FROM && a.D / 8 <= 4 * RMSN_BWD_NTMAX)
+        wide_shape(a.D / 8, 512, &c.bwd_threads, &c.bwd_vpt);
     cudaError_t e;
     if (is_f16(m)) e = c.narrow ? launch_narrow_bwd_f16(m, a, c, s) : launch_wide_bwd_f16(m, a, c, s);
     else e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);

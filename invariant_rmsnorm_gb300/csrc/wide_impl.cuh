@@ -60,6 +60,9 @@
 #ifndef RMSN_WIDE_BWD_CTAS_PER_SM
 #define RMSN_WIDE_BWD_CTAS_PER_SM 2
 #endif
+#ifndef RMSN_WIDE_BWD_SMEM_512
+#define RMSN_WIDE_BWD_SMEM_512 (96 * 1024)  // ring budget of the 512-thread backward (one CTA per SM)
+#endif
 #ifndef RMSN_MAX_STAGES
 #define RMSN_MAX_STAGES 16
 #endif
@@ -751,7 +754,7 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     constexpr int R = bwd_rows<VPT, MAXT>();
     const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
     const size_t fixed = 2 * R * 32 * 4;
-    const int S = stages_for(RMSN_WIDE_BWD_SMEM, stage, 16 + 4 * R, fixed);
+    const int S = stages_for(MAXT > 256 ? RMSN_WIDE_BWD_SMEM_512 : RMSN_WIDE_BWD_SMEM, stage, 16 + 4 * R, fixed);
     const size_t smem = S * (stage + 16 + 4 * R) + fixed;
     if (smem > static_cast<size_t>(kMaxSmemPerCta)) return cudaErrorInvalidConfiguration;
     const int threads = c.bwd_threads + 32;

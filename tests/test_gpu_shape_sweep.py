@@ -23,7 +23,8 @@ pytestmark = pytest.mark.gpu
 
 # Boundaries of the launch shapes (in elements): narrow groups (<= 256), wide
 # VPT 1 (<= 2048 at 256 threads), VPT 2 (<= 4096), VPT 4 on <= 224 threads
-# (<= 7168), on 256 (<= 8192), on 512 threads (> 8192).
+# (<= 7168), then up to 8192 the forward's VPT 4 on 256 threads and the
+# backward's VPT 2 on 512, and VPT 4 on 512 threads beyond.
 BOUNDARY_D = [8, 16, 136, 256, 264, 2048, 2056, 4096, 4104, 7168, 7176, 8192, 8200, 16384]
 
 
