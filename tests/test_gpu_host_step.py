@@ -122,3 +122,35 @@ def test_host_step_back_to_back_on_one_stream():
     s.synchronize()
     for i, ((x, g, gr, w), (o, _)) in enumerate(zip(cases, outs)):
         _assert_same(o, _device_step(x, g, gr, w, False), f"call {i}")
+
+
+def test_host_step_in_a_cuda_graph():
+    """Captured in a CUDA graph, after one call outside capture has created the
+    library's copy streams: the copy streams fork from and join the captured
+    stream, and every replay gives the device entry points' bits."""
+    T, D = 1000, 512
+    x, g, gr, w = _inputs(T, D, 77, torch.bfloat16, False)
+    dev = _device_step(x, g, gr, w, False)
+    hx, hg, hgr, hw = (t.cpu().pin_memory() for t in (x, g, gr, w))
+    o = {"y": torch.empty((T, D), dtype=x.dtype, pin_memory=True),
+         "x_copy": torch.empty((T, D), dtype=x.dtype, pin_memory=True),
+         "rstd": torch.empty(T, pin_memory=True), "dx": torch.empty((T, D), dtype=x.dtype, pin_memory=True),
+         "dgamma": torch.empty(D, pin_memory=True)}
+    work = torch.empty(rn.rmsnorm_residual_step_host_work_bytes(T, D, 128), dtype=torch.uint8, device=DEV)
+    s = torch.cuda.Stream()
+
+    def call():
+        rn.rmsnorm_residual_step_host(hx, hg, hgr, hw, o["y"], o["x_copy"], o["rstd"], o["dx"], o["dgamma"], work,
+                                      EPS, False, slab_rows=128, stream=s)
+
+    call()
+    s.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=s):
+        call()
+    for rep in range(3):
+        for t in o.values():
+            t.zero_()
+        graph.replay()
+        torch.cuda.synchronize()
+        _assert_same(o, dev, f"graph replay {rep}")
