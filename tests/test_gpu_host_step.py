@@ -154,3 +154,45 @@ def test_host_step_in_a_cuda_graph():
         graph.replay()
         torch.cuda.synchronize()
         _assert_same(o, dev, f"graph replay {rep}")
+
+
+def test_host_step_from_two_host_threads():
+    """Two host threads, each with its own stream, work buffer and inputs, call
+    the step three times each at the same time (the binding releases the GIL
+    in the call): the library serialises their enqueueing on its shared copy
+    streams, and every result is the device entry points'."""
+    import threading
+    T, D = 1500, 1024
+    cases = [_inputs(T, D, 90 + i, torch.bfloat16, i == 1) for i in range(2)]
+    refs = [_device_step(x, g, gr, w, i == 1) for i, (x, g, gr, w) in enumerate(cases)]
+    results, errors = [[], []], []
+
+    def worker(i):
+        try:
+            x, g, gr, w = cases[i]
+            hx, hg, hgr, hw = (t.cpu().pin_memory() for t in (x, g, gr, w))
+            s = torch.cuda.Stream()
+            work = torch.empty(rn.rmsnorm_residual_step_host_work_bytes(T, D, 256), dtype=torch.uint8, device=DEV)
+            for _ in range(3):
+                o = {"y": torch.empty((T, D), dtype=x.dtype, pin_memory=True),
+                     "x_copy": torch.empty((T, D), dtype=x.dtype, pin_memory=True),
+                     "rstd": torch.empty(T, pin_memory=True),
+                     "dx": torch.empty((T, D), dtype=x.dtype, pin_memory=True),
+                     "dgamma": torch.empty(D, pin_memory=True)}
+                rn.rmsnorm_residual_step_host(hx, hg, hgr, hw, o["y"], o["x_copy"], o["rstd"], o["dx"], o["dgamma"],
+                                              work, EPS, i == 1, slab_rows=256, stream=s)
+                results[i].append(o)
+            s.synchronize()
+        except Exception as e:  # reported by the main thread
+            errors.append(e)
+
+    threads = [threading.Thread(target=worker, args=(i,)) for i in range(2)]
+    for t in threads:
+        t.start()
+    for t in threads:
+        t.join(timeout=120)
+    assert not errors, errors
+    for i in range(2):
+        assert len(results[i]) == 3
+        for k, o in enumerate(results[i]):
+            _assert_same(o, refs[i], f"thread {i} call {k}")
