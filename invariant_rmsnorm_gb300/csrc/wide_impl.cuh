@@ -453,6 +453,12 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // (D <= 8192) both cost more than they save.
     constexpr bool HOLD = VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE;
     constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
+    // Element pairs through the packed fp32 instructions (same bits as the
+    // scalar loops) in the two-vector kernels on 128 and on 512 threads, where
+    // they measured faster (131072 x 2048: 282 -> 259 us; 131072 x 8192:
+    // 1101 -> 1060 us). The 256-thread two-vector kernel (D = 4096) and the
+    // four-vector kernels measured slower with them and keep scalar loops.
+    constexpr bool X2 = VPT == 2 && (MAXT == 128 || MAXT > 256) && RMSN_F32X2;
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -594,11 +600,27 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                 gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));  // g*q(z)
                             }
                         }
+                        if constexpr (X2) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            gw[r][j][e] = fmul(gf[e], wj[e]);
-                            if (!RMSN_BWD_LEAN) gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
-                            sp[r] = fadd(sp[r], fmul(gw[r][j][e], xs[r][j][e]));
+                            for (int e = 0; e < 8; e += 2) {  // element pairs; s in ascending element order
+                                const float2 gw2 = fmul2(pair(gf, e), pair(wj, e));
+                                gw[r][j][e] = gw2.x;
+                                gw[r][j][e + 1] = gw2.y;
+                                if (!RMSN_BWD_LEAN) {
+                                    const float2 gx2 = fmul2(pair(gf, e), pair(xs[r][j], e));
+                                    gx[r][j][e] = gx2.x;
+                                    gx[r][j][e + 1] = gx2.y;
+                                }
+                                const float2 t2 = fmul2(gw2, pair(xs[r][j], e));
+                                sp[r] = fadd(fadd(sp[r], t2.x), t2.y);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                gw[r][j][e] = fmul(gf[e], wj[e]);
+                                if (!RMSN_BWD_LEAN) gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
+                                sp[r] = fadd(sp[r], fmul(gw[r][j][e], xs[r][j][e]));
+                            }
                         }
                     }
                 }
@@ -639,36 +661,87 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             unpack_act<F16>(gv[r][j], gf);
                             norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
                             if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) {
+                            if constexpr (X2) {
                                 if (M == kGated) {
-                                    g0[r][j][e] = gf[e];
-                                    gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));
+#pragma unroll
+                                    for (int e = 0; e < 8; ++e) {
+                                        g0[r][j][e] = gf[e];
+                                        gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));
+                                    }
                                 }
-                                gw[r][j][e] = fmul(gf[e], wj[e]);
-                                gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
+#pragma unroll
+                                for (int e = 0; e < 8; e += 2) {
+                                    const float2 gw2 = fmul2(pair(gf, e), pair(wj, e));
+                                    const float2 gx2 = fmul2(pair(gf, e), pair(xs[r][j], e));
+                                    gw[r][j][e] = gw2.x;
+                                    gw[r][j][e + 1] = gw2.y;
+                                    gx[r][j][e] = gx2.x;
+                                    gx[r][j][e + 1] = gx2.y;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    if (M == kGated) {
+                                        g0[r][j][e] = gf[e];
+                                        gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));
+                                    }
+                                    gw[r][j][e] = fmul(gf[e], wj[e]);
+                                    gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
+                                }
                             }
                         }
                         float o[8], fg[8];
                         if (M == kFusedAdd) unpack_act<F16>(fv[r][j], fg);
+                        if constexpr (X2) {
+                            const float2 r2 = both(r1), c2 = both(coef);
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            float d = fsub(fmul(gw[r][j][e], r1), fmul(xs[r][j][e], coef));
-                            if (M == kResidual) d = fadd(d, tz[r][j][e]);
-                            if (M == kFusedAdd) d = fadd(d, fg[e]);
-                            o[e] = d;
-                            acc[j][e] = fadd(acc[j][e], fmul(gx[r][j][e], r1));
+                            for (int e = 0; e < 8; e += 2) {  // element pairs (products packed, their sums scalar)
+                                const float2 p2 = fmul2(pair(gw[r][j], e), r2), q2 = fmul2(pair(xs[r][j], e), c2);
+                                float2 d = make_float2(fsub(p2.x, q2.x), fsub(p2.y, q2.y));
+                                if (M == kResidual) d = fadd2(d, pair(tz[r][j], e));
+                                if (M == kFusedAdd) d = fadd2(d, pair(fg, e));
+                                o[e] = d.x;
+                                o[e + 1] = d.y;
+                                const float2 t2 = fmul2(pair(gx[r][j], e), r2);
+                                acc[j][e] = fadd(acc[j][e], t2.x);
+                                acc[j][e + 1] = fadd(acc[j][e + 1], t2.y);
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) {
+                                float d = fsub(fmul(gw[r][j][e], r1), fmul(xs[r][j][e], coef));
+                                if (M == kResidual) d = fadd(d, tz[r][j][e]);
+                                if (M == kFusedAdd) d = fadd(d, fg[e]);
+                                o[e] = d;
+                                acc[j][e] = fadd(acc[j][e], fmul(gx[r][j][e], r1));
+                            }
                         }
                         st_global_cs(dxrow + 8 * v, pack_act<F16>(o));
                         if (M == kGated) {
                             float dzv[8], yv[8];
+                            if constexpr (X2) {
+                                float q[8], dq[8];
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) {
-                                float q, dq;
-                                gate_eval<SIG>(tz[r][j][e], q, dq);
-                                const float u = fmul(fmul(xs[r][j][e], r1), wj[e]);
-                                dzv[e] = fmul(fmul(g0[r][j][e], u), dq);
-                                yv[e] = fmul(u, q);
+                                for (int e = 0; e < 8; ++e) gate_eval<SIG>(tz[r][j][e], q[e], dq[e]);
+#pragma unroll
+                                for (int e = 0; e < 8; e += 2) {
+                                    const float2 u = fmul2(fmul2(pair(xs[r][j], e), both(r1)), pair(wj, e));
+                                    const float2 dz2 = fmul2(fmul2(pair(g0[r][j], e), u), pair(dq, e));
+                                    const float2 y2 = fmul2(u, pair(q, e));
+                                    dzv[e] = dz2.x;
+                                    dzv[e + 1] = dz2.y;
+                                    yv[e] = y2.x;
+                                    yv[e + 1] = y2.y;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    float q, dq;
+                                    gate_eval<SIG>(tz[r][j][e], q, dq);
+                                    const float u = fmul(fmul(xs[r][j][e], r1), wj[e]);
+                                    dzv[e] = fmul(fmul(g0[r][j][e], u), dq);
+                                    yv[e] = fmul(u, q);
+                                }
                             }
                             st_global_cs(a.dz + row * a.lddz + 8 * v, pack_act<F16>(dzv));
                             if (a.y) st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
@@ -676,8 +749,17 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             // The forward output again, from the saved rstd: same operations,
                             // same bits as the forward's y.
                             float yv[8];
+                            if constexpr (X2) {
 #pragma unroll
-                            for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), wj[e]);
+                                for (int e = 0; e < 8; e += 2) {
+                                    const float2 y2 = fmul2(fmul2(pair(xs[r][j], e), both(r1)), pair(wj, e));
+                                    yv[e] = y2.x;
+                                    yv[e + 1] = y2.y;
+                                }
+                            } else {
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), wj[e]);
+                            }
                             st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
                         }
                     }
