@@ -454,11 +454,15 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr bool HOLD = VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE;
     constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
     // Element pairs through the packed fp32 instructions (same bits as the
-    // scalar loops) in the two-vector kernels on 128 and on 512 threads, where
-    // they measured faster (131072 x 2048: 282 -> 259 us; 131072 x 8192:
-    // 1101 -> 1060 us). The 256-thread two-vector kernel (D = 4096) and the
-    // four-vector kernels measured slower with them and keep scalar loops.
+    // scalar loops), where they measured faster: every site of the two-vector
+    // kernels on 128 and on 512 threads (131072 x 2048: 282 -> 259 us;
+    // 131072 x 8192: 1101 -> 1060 us), and the outputs after the reduction in
+    // the 256-thread one (D = 4096 plain: 132.7 -> 129.9 us; residual equal).
+    // Pairs before the reduction or in its recompute made that kernel slower,
+    // and the four-vector kernels slower at every site.
     constexpr bool X2 = VPT == 2 && (MAXT == 128 || MAXT > 256) && RMSN_F32X2;
+    constexpr bool X2P1 = X2, X2RC = X2;            // before the reduction; its recompute
+    constexpr bool X2OUT = VPT == 2 && RMSN_F32X2;  // dx, the weight-gradient term, dz and y
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -600,7 +604,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                 gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));  // g*q(z)
                             }
                         }
-                        if constexpr (X2) {
+                        if constexpr (X2P1) {
 #pragma unroll
                             for (int e = 0; e < 8; e += 2) {  // element pairs; s in ascending element order
                                 const float2 gw2 = fmul2(pair(gf, e), pair(wj, e));
@@ -661,7 +665,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             unpack_act<F16>(gv[r][j], gf);
                             norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
                             if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
-                            if constexpr (X2) {
+                            if constexpr (X2RC) {
                                 if (M == kGated) {
 #pragma unroll
                                     for (int e = 0; e < 8; ++e) {
@@ -692,7 +696,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         }
                         float o[8], fg[8];
                         if (M == kFusedAdd) unpack_act<F16>(fv[r][j], fg);
-                        if constexpr (X2) {
+                        if constexpr (X2OUT) {
                             const float2 r2 = both(r1), c2 = both(coef);
 #pragma unroll
                             for (int e = 0; e < 8; e += 2) {  // element pairs (products packed, their sums scalar)
@@ -719,7 +723,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         st_global_cs(dxrow + 8 * v, pack_act<F16>(o));
                         if (M == kGated) {
                             float dzv[8], yv[8];
-                            if constexpr (X2) {
+                            if constexpr (X2OUT) {
                                 float q[8], dq[8];
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) gate_eval<SIG>(tz[r][j][e], q[e], dq[e]);
@@ -749,7 +753,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             // The forward output again, from the saved rstd: same operations,
                             // same bits as the forward's y.
                             float yv[8];
-                            if constexpr (X2) {
+                            if constexpr (X2OUT) {
 #pragma unroll
                                 for (int e = 0; e < 8; e += 2) {
                                     const float2 y2 = fmul2(fmul2(pair(xs[r][j], e), both(r1)), pair(wj, e));
