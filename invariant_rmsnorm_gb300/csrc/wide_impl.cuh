@@ -456,13 +456,16 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // Element pairs through the packed fp32 instructions (same bits as the
     // scalar loops), where they measured faster: every site of the two-vector
     // kernels on 128 and on 512 threads (131072 x 2048: 282 -> 259 us;
-    // 131072 x 8192: 1101 -> 1060 us), and the outputs after the reduction in
-    // the 256-thread one (D = 4096 plain: 132.7 -> 129.9 us; residual equal).
-    // Pairs before the reduction or in its recompute made that kernel slower,
-    // and the four-vector kernels slower at every site.
-    constexpr bool X2 = VPT == 2 && (MAXT == 128 || MAXT > 256) && RMSN_F32X2;
-    constexpr bool X2P1 = X2, X2RC = X2;            // before the reduction; its recompute
-    constexpr bool X2OUT = VPT == 2 && RMSN_F32X2;  // dx, the weight-gradient term, dz and y
+    // 131072 x 8192: 1101 -> 1060 us) and of the one-vector kernel in the
+    // gated and fused-add modes (131072 x 2048: 605 -> 585 us, 407 -> 402 us),
+    // and the outputs after the reduction in the 256-thread two-vector kernel
+    // (D = 4096 plain: 132.7 -> 129.9 us; residual equal). Pairs elsewhere in
+    // that kernel, in the one-vector residual backward (336 -> 341 us) and in
+    // the four-vector kernels measured slower.
+    constexpr bool V1X2 = VPT == 1 && (M == kGated || M == kFusedAdd);
+    constexpr bool X2 = ((VPT == 2 && (MAXT == 128 || MAXT > 256)) || V1X2) && RMSN_F32X2;
+    constexpr bool X2P1 = X2, X2RC = X2;                      // before the reduction; its recompute
+    constexpr bool X2OUT = (VPT == 2 || V1X2) && RMSN_F32X2;  // dx, the weight-gradient term, dz and y
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
