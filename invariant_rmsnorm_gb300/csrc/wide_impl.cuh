@@ -273,11 +273,12 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
     constexpr bool SIG = is_sigmoid_gate(MODE);
     static_assert(!(M == kGatedHF && F16), "the HF-convention witness is a bf16 forward");
     // Element pairs through the packed fp32 instructions (same bits as the
-    // scalar loops) in the one-vector kernel (D <= 2048; 131072 x 2048 plain:
-    // 175.9 -> 171.4 us). With two or four vectors a thread they measured
-    // slower (D = 4096: 347 -> 362 us; 16384: 338 -> 357 us).
-    constexpr bool FX2P = RMSN_F32X2 && VPT == 1;  // the squares of the sum of squares
-    constexpr bool FX2O = RMSN_F32X2 && VPT == 1;  // the output products
+    // scalar loops) in the one-vector kernel outside the gated mode (D <= 2048;
+    // 131072 x 2048 plain 175.7 -> 171.1 us, residual 272.6 -> 271.0, fused
+    // add 376.4 -> 374.6; gated measured 303.1 -> 309.4). With two or four
+    // vectors a thread they measured slower (D = 4096: 347 -> 362 us).
+    constexpr bool FX2P = RMSN_F32X2 && VPT == 1 && M != kGated;  // the squares of the sum of squares
+    constexpr bool FX2O = FX2P;                                   // the output products
     constexpr int NIN = fwd_inputs(MODE);
     constexpr int R = fwd_rows<VPT, MAXT, MODE>();
     constexpr int NWMAX = MAXT / 32;
