@@ -194,3 +194,40 @@ def assert_dgamma_parity(name, got, ref, abs_sum, chunk_rows: int, nchunks: int)
         raise AssertionError(f"{name}: {np.count_nonzero(~ok)} columns outside tolerance; first {i}: "
                              f"got {got[i]!r} ref {ref[i]!r} sum|t| {abs_sum[i]!r}")
     return int(np.count_nonzero(m2 & ~m1))
+
+
+WIDE_CHUNK_ROWS = 32    # weight-gradient chunk of the wide path (D > 256)
+PASS2_RANGES = 32       # pass-2 ranges of contiguous chunks
+
+
+def dgamma_model(g, h, r, fused: bool = False):
+    """float32 model of the wide backward's weight gradient: ((g*h)*r) per
+    element, each multiply and add rounded to fp32, ascending rows within each
+    32-row chunk, then the chunk partials through the pass-2 tree (32
+    contiguous ranges of ceil(n/32) chunks in ascending order, the range totals
+    in order). g, h [T, D] and r [T] are float32 and exact. With fused=True the
+    per-row update is a fused multiply-add instead (acc + gx*r rounded once),
+    the rounding the kernels must not do."""
+    T, D = g.shape
+    nch = -(-T // WIDE_CHUNK_ROWS)
+    partials = np.zeros((nch, D), np.float32)
+    for c in range(nch):
+        acc = np.zeros(D, np.float32)
+        for t in range(c * WIDE_CHUNK_ROWS, min(T, (c + 1) * WIDE_CHUNK_ROWS)):
+            gx = g[t] * h[t]
+            if fused:
+                acc = (gx.astype(np.float64) * np.float64(r[t]) + acc.astype(np.float64)).astype(np.float32)
+            else:
+                acc = acc + gx * r[t]
+        partials[c] = acc
+    per = -(-nch // PASS2_RANGES)
+    totals = []
+    for w in range(PASS2_RANGES):
+        s = np.zeros(D, np.float32)
+        for c in range(w * per, min(nch, (w + 1) * per)):
+            s = s + partials[c]
+        totals.append(s)
+    out = totals[0]
+    for w in range(1, PASS2_RANGES):
+        out = out + totals[w]
+    return out
