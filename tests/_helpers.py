@@ -200,26 +200,9 @@ WIDE_CHUNK_ROWS = 32    # weight-gradient chunk of the wide path (D > 256)
 PASS2_RANGES = 32       # pass-2 ranges of contiguous chunks
 
 
-def dgamma_model(g, h, r, fused: bool = False):
-    """float32 model of the wide backward's weight gradient: ((g*h)*r) per
-    element, each multiply and add rounded to fp32, ascending rows within each
-    32-row chunk, then the chunk partials through the pass-2 tree (32
-    contiguous ranges of ceil(n/32) chunks in ascending order, the range totals
-    in order). g, h [T, D] and r [T] are float32 and exact. With fused=True the
-    per-row update is a fused multiply-add instead (acc + gx*r rounded once),
-    the rounding the kernels must not do."""
-    T, D = g.shape
-    nch = -(-T // WIDE_CHUNK_ROWS)
-    partials = np.zeros((nch, D), np.float32)
-    for c in range(nch):
-        acc = np.zeros(D, np.float32)
-        for t in range(c * WIDE_CHUNK_ROWS, min(T, (c + 1) * WIDE_CHUNK_ROWS)):
-            gx = g[t] * h[t]
-            if fused:
-                acc = (gx.astype(np.float64) * np.float64(r[t]) + acc.astype(np.float64)).astype(np.float32)
-            else:
-                acc = acc + gx * r[t]
-        partials[c] = acc
+def _pass2(partials):
+    """The fixed pass-2 tree over chunk partials [n, D] (float32)."""
+    nch, D = partials.shape
     per = -(-nch // PASS2_RANGES)
     totals = []
     for w in range(PASS2_RANGES):
@@ -231,3 +214,57 @@ def dgamma_model(g, h, r, fused: bool = False):
     for w in range(1, PASS2_RANGES):
         out = out + totals[w]
     return out
+
+
+def _accumulate(acc, gx, rt, fused):
+    if fused:
+        return (gx.astype(np.float64) * np.float64(rt) + acc.astype(np.float64)).astype(np.float32)
+    return acc + gx * rt
+
+
+def dgamma_model(g, h, r, fused: bool = False):
+    """float32 model of the weight gradient: ((g*h)*r) per element, each
+    multiply and add rounded to fp32, summed per chunk in the order the path
+    fixes, then the chunk partials through the pass-2 tree (32 contiguous
+    ranges of ceil(n/32) chunks in ascending order, the range totals in order).
+    g, h [T, D] and r [T] are float32 and exact. D > 256 (wide path): 32-row
+    chunks, rows in ascending order. D <= 256 (narrow path): G = next power of
+    two of D/8 lanes per row, P = 256/G rows per pass, stages of RS = 32 rows
+    (P if larger; 32 when G = 32), chunks of max(RS, 128) rows; lane group q
+    adds the rows chunk + s*RS + p*P + q, stage by stage and pass by pass, and
+    the chunk partial is the group totals added in group order. With
+    fused=True the per-row update is a fused multiply-add instead (acc + gx*r
+    rounded once), the rounding the kernels must not do."""
+    T, D = g.shape
+    if D > 256:
+        nch = -(-T // WIDE_CHUNK_ROWS)
+        partials = np.zeros((nch, D), np.float32)
+        for c in range(nch):
+            acc = np.zeros(D, np.float32)
+            for t in range(c * WIDE_CHUNK_ROWS, min(T, (c + 1) * WIDE_CHUNK_ROWS)):
+                acc = _accumulate(acc, g[t] * h[t], r[t], fused)
+            partials[c] = acc
+        return _pass2(partials)
+    G = 1
+    while G < D // 8:
+        G *= 2
+    P = 256 // G
+    RS = 32 if G == 32 else max(P, 32)
+    CN = max(RS, 128)
+    nch = -(-T // CN)
+    partials = np.zeros((nch, D), np.float32)
+    for c in range(nch):
+        groups = []
+        for q in range(P):
+            acc = np.zeros(D, np.float32)
+            for st in range(CN // RS):
+                for p in range(RS // P):
+                    t = c * CN + st * RS + p * P + q
+                    if t < T:
+                        acc = _accumulate(acc, g[t] * h[t], r[t], fused)
+            groups.append(acc)
+        tot = groups[0]
+        for q in range(1, P):
+            tot = tot + groups[q]
+        partials[c] = tot
+    return _pass2(partials)

@@ -1,4 +1,4 @@
-"""The float32 model of the wide weight gradient (tests/_helpers.py), which the
+"""The float32 model of the weight gradient (tests/_helpers.py), which the
 GPU test holds the kernels to bit for bit, checked on the CPU: it agrees with
 the float64 oracle within the weight gradient's tolerance, and it can tell
 separately rounded arithmetic from a fused multiply-add on ordinary inputs, so
@@ -6,6 +6,7 @@ a kernel that fused would fail the GPU test."""
 from __future__ import annotations
 
 import numpy as np
+import pytest
 
 import oracle
 from tests._helpers import dgamma_model
@@ -19,8 +20,9 @@ def _inputs(T, D, seed):
     return g, x, r
 
 
-def test_model_matches_the_oracle_within_tolerance():
-    T, D = 1100, 264
+@pytest.mark.parametrize("D", [64, 264])
+def test_model_matches_the_oracle_within_tolerance(D):
+    T = 1100
     g, x, r = _inputs(T, D, 5)
     got = dgamma_model(g, x, r).astype(np.float64)
     w = np.ones(D)
@@ -29,8 +31,9 @@ def test_model_matches_the_oracle_within_tolerance():
     assert np.all(np.abs(got - want) <= 1e-4 * np.abs(want) + 1e-6 * absum)
 
 
-def test_model_separates_fused_from_separate_rounding():
-    T, D = 300, 1000
+@pytest.mark.parametrize("D", [128, 1000])
+def test_model_separates_fused_from_separate_rounding(D):
+    T = 300
     g, x, r = _inputs(T, D, 9)
     a = dgamma_model(g, x, r)
     b = dgamma_model(g, x, r, fused=True)

@@ -1,11 +1,12 @@
-"""The weight gradient of the wide backward, bit for bit against a float32
+"""The weight gradient of the backward, bit for bit against a float32
 model of its stated arithmetic.
 
 Per RL-Kernel pull request 414 "[DSv4][P1-5] rmsnorm_residual" (Implementation:
 ascending fp32 reductions, every multiply and add rounded on its own, no
 atomics), dgamma_j is built from the products ((g_tj * x_tj) * r_t), each
 rounded to fp32, added in ascending row order within each 32-row chunk (pass 1),
-and the chunk partials added by the fixed pass-2 tree: 32 contiguous ranges of
+(wide path; the narrow path's order is described below), and the chunk
+partials added by the fixed pass-2 tree: 32 contiguous ranges of
 ceil(n / 32) chunks, each summed in ascending order, then the 32 range totals
 in order. Every operand here is exact in fp32 (bf16 or fp16 activations, the
 rstd given as input), so numpy's float32 operations reproduce each rounding,
@@ -13,10 +14,13 @@ and any fused multiply-add anywhere in the kernel, or any change of order,
 changes bits. The gated mode is left out: its products involve the gate,
 which the kernel evaluates with the hardware exponential.
 
-Widths cover every backward launch shape of the wide path: one vector a
-thread (264, 1000, and 2048 outside the plain mode), two vectors on 128
-threads (2048 plain), on 256 (4096) and on 512 (8192), four vectors on 224
-(7168) and on 512 threads (16384).
+Widths cover every backward launch shape: on the narrow path (D <= 256),
+lane groups of 1, 2, 8, 16 and 32 lanes a row, whose chunk order is its own
+(lane groups over interleaved rows, then the group totals in order; see
+dgamma_model); on the wide path one vector a thread (264, 1000, and 2048
+outside the plain mode), two vectors on 128 threads (2048 plain), on 256
+(4096) and on 512 (8192), four vectors on 224 (7168) and on 512 threads
+(16384).
 """
 from __future__ import annotations
 
@@ -36,7 +40,9 @@ def _f32(t):
     return t.detach().float().cpu().numpy().astype(np.float32)
 
 
-CASES = [(D, T) for D in (264, 1000, 2048, 4096, 7168, 8192, 16384) for T in (100, 1100)]
+WIDE = [(D, T) for D in (264, 1000, 2048, 4096, 7168, 8192, 16384) for T in (100, 1100)]
+NARROW = [(D, T) for D in (8, 16, 40, 64, 128, 200, 256) for T in (100, 1100)]  # lane groups of 1 to 32
+CASES = NARROW + WIDE
 
 
 @pytest.mark.parametrize("variant", ["plain", "residual", "fused"])
