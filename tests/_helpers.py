@@ -268,3 +268,94 @@ def dgamma_model(g, h, r, fused: bool = False):
             tot = tot + groups[q]
         partials[c] = tot
     return _pass2(partials)
+
+
+def f32_round_act(v, fmt: str = "bf16") -> np.ndarray:
+    """float32 values rounded to bf16 or fp16, nearest even, returned as float32."""
+    v = np.asarray(v, np.float32)
+    if fmt == "f16":
+        return v.astype(np.float16).astype(np.float32)
+    bits = v.view(np.uint32).astype(np.uint64)
+    bits = (bits + 0x7FFF + ((bits >> 16) & 1)) & 0xFFFF0000
+    return bits.astype(np.uint32).view(np.float32)
+
+
+def bwd_row_shape(D: int, mode: str):
+    """Consumer threads and 16-byte vectors a thread of the wide backward's row
+    reduction, a function of D and the mode: up to 256 threads (512 beyond 1024
+    vectors), 1, 2 or 4 vectors each; plain rows of at most 256 vectors on at most
+    128 threads; rows of 897..1024 vectors on 512 threads."""
+    NV = D // 8
+
+    def shape(ntmax):
+        if NV > 4 * ntmax:
+            ntmax = 512
+        need = -(-NV // ntmax)
+        vpt = 1 if need <= 1 else (2 if need <= 2 else 4)
+        return -(-(-(-NV // vpt)) // 32) * 32, vpt
+
+    nt, vpt = shape(256)
+    if mode == "plain" and NV <= 256:
+        nt, vpt = shape(128)
+    if 897 <= NV <= 1024:
+        nt, vpt = shape(512)
+    return nt, vpt
+
+
+def row_sums_model(terms, D: int, mode: str):
+    """The fixed row reduction of [T, D] float32 terms: on the wide path each
+    consumer thread t adds its elements (vectors v = j*NT + t, j ascending, the 8
+    elements of each in order) from 0, an xor butterfly over each warp (offsets
+    16..1) gives every lane the warp total, and the warp totals are added in
+    warp order; on the narrow path (D <= 256) each lane of a row's group of
+    G = next_pow2(D/8) lanes adds its 8 elements and a butterfly over the group
+    (offsets G/2..1) gives the total."""
+    T = terms.shape[0]
+    NV = D // 8
+    vec = terms.reshape(T, NV, 8)
+    if D <= 256:
+        G = 1
+        while G < NV:
+            G *= 2
+        lanes = np.zeros((T, G), np.float32)
+        for e in range(8):
+            lanes[:, :NV] = lanes[:, :NV] + vec[:, :, e]
+        o = G // 2
+        while o > 0:
+            lanes = lanes + lanes[:, np.arange(G) ^ o]
+            o //= 2
+        return lanes[:, 0]
+    nt, vpt = bwd_row_shape(D, mode)
+    th = np.zeros((T, nt), np.float32)
+    for j in range(vpt):
+        for t0 in range(nt):
+            v = j * nt + t0
+            if v < NV:
+                for e in range(8):
+                    th[:, t0] = th[:, t0] + vec[:, v, e]
+    nw = nt // 32
+    warps = th.reshape(T, nw, 32)
+    o = 16
+    while o > 0:
+        warps = warps + warps[:, :, np.arange(32) ^ o]
+        o //= 2
+    s = warps[:, 0, 0]
+    for i in range(1, nw):
+        s = s + warps[:, i, 0]
+    return s
+
+
+def dx_model(g, h, w_eff, r, mode: str, g_res=None, fmt: str = "bf16"):
+    """The backward's input gradient, modelled in float32 and rounded once:
+    s = fixed row sum of ((g*w_eff)*h); coef = (((r*r)*r) / D) * s (a power-of-two D
+    scales by its exact reciprocal); dx = ((g*w_eff)*r) - (h*coef) [+ g_res]."""
+    T, D = g.shape
+    gw = g * w_eff[None, :]
+    s = row_sums_model(gw * h, D, mode)
+    r3 = (r * r) * r
+    q = r3 * np.float32(1.0 / D) if (D & (D - 1)) == 0 else r3 / np.float32(D)
+    coef = q * s
+    d = gw * r[:, None] - h * coef[:, None]
+    if g_res is not None:
+        d = d + g_res
+    return f32_round_act(d, fmt)

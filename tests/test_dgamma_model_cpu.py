@@ -39,3 +39,30 @@ def test_model_separates_fused_from_separate_rounding(D):
     b = dgamma_model(g, x, r, fused=True)
     differ = np.count_nonzero(a.view(np.uint32) != b.view(np.uint32))
     assert differ > D // 10, differ   # most columns tell the two apart
+
+
+@pytest.mark.parametrize("D", [128, 264, 4096])
+def test_dx_model_matches_the_oracle(D):
+    """The dx model (fixed row tree, fp32 steps, one rounding) is within the
+    contract's bound of the float64 oracle: one ulp, or the cancellation bound."""
+    from tests._helpers import assert_bf16_parity, dx_model
+    T = 40
+    g, x, r = _inputs(T, D, 13)
+    w = (1.0 + 0.1 * np.random.default_rng(14).standard_normal(D)).astype(np.float32)
+    got = dx_model(g, x, w, r, "plain").astype(np.float64)
+    dx, _, diag = oracle.rmsnorm_bwd(g.astype(np.float64), x.astype(np.float64), w.astype(np.float64),
+                                     r.astype(np.float64), False, diagnostics=True)
+    assert_bf16_parity(f"dx model D={D}", got, dx, diag["dx_pre"], diag["dx_scale"])
+
+
+def test_row_sum_model_tree_is_not_a_plain_sum():
+    """The row tree of the model differs from a left-to-right sum on ordinary
+    inputs, so the GPU test pins the kernels' tree, not just the total."""
+    from tests._helpers import row_sums_model
+    rng = np.random.default_rng(3)
+    terms = rng.standard_normal((64, 4096)).astype(np.float32)
+    tree = row_sums_model(terms, 4096, "residual")
+    seq = np.zeros(64, np.float32)
+    for k in range(4096):
+        seq = seq + terms[:, k]
+    assert np.count_nonzero(tree.view(np.uint32) != seq.view(np.uint32)) > 16
