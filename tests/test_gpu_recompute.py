@@ -1,6 +1,7 @@
-"""Backward with recomputation of the forward output (SURVEY's "single pass
-for recompute" row): the y it writes is the forward's y bit for bit, and its
-dx / dz / dgamma are those of the plain backward bit for bit."""
+"""Backward with recomputation of the forward output (one pass that writes y
+again for activation recomputation, instead of a separate forward): the y it
+writes is the forward's y bit for bit, and its dx / dz / dgamma are those of
+the plain backward bit for bit."""
 from __future__ import annotations
 
 import pytest
