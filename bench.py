@@ -38,6 +38,13 @@ METRIC = "RMSNorm fwd+bwd HBM GB/s (% of GB300 peak) at T=32768, D=4096, bf16"
 PAGES_H100_CUDA_MS = 10.043916  # residual fwd+bwd, T=32768, D=4096, H100 PCIe (context only)
 
 
+def residual_config(world):
+    """The benchmark's workload, the same for both arms."""
+    return {"workload": "rmsnorm_residual fwd+bwd", "T": T_ROWS, "D": D_COLS,
+            "io": "bf16 activations, fp32 gamma/rstd/dgamma", "eps": EPS, "zero_centered_gamma": False,
+            "parallelism": f"replicas x{world}", "l2": "inputs 1.88 GB per step, larger than L2; no flush"}
+
+
 def step_bytes(T, D):
     return T * (14 * D + 8)
 
@@ -269,9 +276,7 @@ def run_ours(args):
             "vs_baseline": round((PAGES_H100_CUDA_MS / ms_per_step) * world, 3),
             "vs_baseline_basis": "pages' H100 PCIe residual fwd+bwd at the same shape (10.043916 ms); context only",
             "dtype": "f32", "data": "synthetic",
-            "config": {"workload": "rmsnorm_residual fwd+bwd", "T": T, "D": D, "io": "bf16 activations, fp32 gamma/rstd/dgamma",
-                       "eps": EPS, "zero_centered_gamma": False, "parallelism": f"replicas x{world}",
-                       "l2": "inputs 1.88 GB per step, larger than L2; no flush"},
+            "config": residual_config(world),
             "pct_of_peak": round(100.0 * value / (world * peak), 2),
             "kernels_ms": {"fwd": round(fwd_ms, 5), "bwd_pass1": round(bwd_ms, 5), "dgamma_pass2": round(red_ms, 5),
                            "sampled_steps": len(evs)},
@@ -553,8 +558,7 @@ def run_reference(args):
         "impl": "reference", "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(1e3 * dt / args.steps, 3),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": "rmsnorm_residual fwd+bwd", "T": T_ROWS, "D": D_COLS,
-                   "sample_rows_per_step": rows},
+        "config": residual_config(world),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"{rows} of {T_ROWS} rows per step, float64 C oracle"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
