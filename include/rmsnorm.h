@@ -36,9 +36,10 @@
  *     8 <= D <= 16384. eps is finite and >= 0. 0 <= T < 2^31; T == 0 returns
  *     RMSN_OK without launching anything.
  *   - Outputs must not overlap inputs or each other.
- *   - The library allocates nothing. Scratch for the weight gradient is the
- *     caller's workspace `ws` of at least rmsnorm_bwd_workspace_bytes(T, D) bytes
- *     (16-byte aligned). The caller owns every buffer.
+ *   - The library allocates no device memory. Scratch for the weight gradient is
+ *     the caller's workspace `ws` of at least rmsnorm_bwd_workspace_bytes(T, D)
+ *     bytes (16-byte aligned). The caller owns every buffer. (The host-buffer step
+ *     creates two copy streams and a few events per device on its first call.)
  *   - Work is enqueued asynchronously on `stream` (NULL = legacy default stream);
  *     calls on one stream execute in order. A call that returns an error has
  *     enqueued nothing.
@@ -367,8 +368,20 @@ int rmsnorm_residual_step_host(const rmsn_act16* x, const rmsn_act16* g, const r
 
 /* Reads the device-side error flags of the current device (OR of all kernels'
  * flags since the last clear) into *flags; clears them if `clear` is non-zero.
- * Synchronises with the device. 0 means no kernel ever gave up on a wait. */
+ * Synchronises with the device. 0 means no kernel ever gave up on a wait;
+ * RMSN_DEVICE_ERR_WAIT_TIMEOUT is set when a wait ran out of time. */
+#define RMSN_DEVICE_ERR_WAIT_TIMEOUT 1u
 int rmsnorm_device_error(unsigned int* flags, int clear);
+
+/* Self-test of the error path above (no counterpart in the pages). Launches one
+ * thread on `stream` that waits, with the kernels' own bounded wait and the limit
+ * `limit_ns` (1 ns .. 1 s), on a fresh mbarrier that nothing ever completes: the
+ * wait runs out, the thread raises RMSN_DEVICE_ERR_WAIT_TIMEOUT, and the kernel
+ * returns normally, leaving the context usable. If `waited_ns` (a DEVICE pointer
+ * to one 8-byte-aligned uint64, or NULL) is given, the time the wait took is
+ * written there. A limit of 0 or above 1 s is RMSN_EINVAL. */
+int rmsnorm_selftest_wait_timeout(unsigned long long limit_ns, unsigned long long* waited_ns,
+                                  rmsn_stream stream);
 
 #ifdef __cplusplus
 }

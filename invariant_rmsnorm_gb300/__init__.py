@@ -35,7 +35,8 @@ __all__ = [
     "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
     "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex", "DTYPE_CODES", "GATE_CODES",
-    "rmsnorm_residual_step_host", "rmsnorm_residual_step_host_work_bytes",
+    "rmsnorm_residual_step_host", "rmsnorm_residual_step_host_work_bytes", "rmsnorm_selftest_wait_timeout",
+    "DEVICE_ERR_WAIT_TIMEOUT",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -47,8 +48,11 @@ EXPORTED_SYMBOLS = (
     "rmsnorm_fwd_ex", "rmsnorm_bwd_ex", "rmsnorm_residual_fwd_ex", "rmsnorm_residual_bwd_ex",
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
     "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex",
-    "rmsnorm_residual_step_host_work_bytes", "rmsnorm_residual_step_host",
+    "rmsnorm_residual_step_host_work_bytes", "rmsnorm_residual_step_host", "rmsnorm_selftest_wait_timeout",
 )
+
+# RMSN_DEVICE_ERR_WAIT_TIMEOUT of include/rmsnorm.h: the flag a wait that ran out of time raises
+DEVICE_ERR_WAIT_TIMEOUT = 1
 
 # enum rmsn_dtype / enum rmsn_gate of include/rmsnorm.h
 DTYPE_CODES = {torch.bfloat16: 0, torch.float16: 1}
@@ -84,6 +88,7 @@ _SIGS = {
                                            _P, _SZ, _I64, _I64, _INT, _P]),
 }
 _SIGS["rmsnorm_residual_step_host_work_bytes"] = (_SZ, [_I64, _I64, _I64])
+_SIGS["rmsnorm_selftest_wait_timeout"] = (_INT, [ctypes.c_ulonglong, _P, _P])
 _SIGS["rmsnorm_residual_step_host"] = (_INT, [_P] * 9 + [_I64, _I64, _F, _INT, _INT, _I64, _P, _SZ, _P])
 # Each *_ex call: the unsuffixed signature with `int dtype` (gated: `int gate, int dtype`) before the stream.
 for _name in ("rmsnorm_fwd", "rmsnorm_bwd", "rmsnorm_residual_fwd", "rmsnorm_residual_bwd",
@@ -547,3 +552,16 @@ def rmsnorm_residual_step_host(x, g, g_res, w, y, x_copy, rstd, dx, dgamma, work
         _ptr(x), _ptr(g), _ptr(g_res), _ptr(w), _ptr(y), _ptr(x_copy), _ptr(rstd), _ptr(dx), _ptr(dgamma),
         T, D, float(eps), int(zero_centered_gamma), _dtype_code(x), int(slab_rows), wp, wb,
         _stream(stream, work.device)))
+
+
+def rmsnorm_selftest_wait_timeout(limit_ns: int, waited_ns: Optional[torch.Tensor] = None, device=None, stream=None):
+    """Runs the bounded-wait error path on purpose: one thread waits, with the
+    kernels' own wait and a limit of ``limit_ns``, on a barrier nothing completes,
+    then raises DEVICE_ERR_WAIT_TIMEOUT (read it with rmsnorm_device_error). If
+    ``waited_ns`` (a CUDA int64 tensor of one element) is given, the time the wait
+    took is written there."""
+    if waited_ns is not None and (not waited_ns.is_cuda or waited_ns.dtype != torch.int64 or waited_ns.numel() != 1):
+        raise TypeError("waited_ns: expected a one-element int64 CUDA tensor")
+    dev = waited_ns.device if waited_ns is not None else (device or torch.device("cuda", torch.cuda.current_device()))
+    _check("rmsnorm_selftest_wait_timeout", load().rmsnorm_selftest_wait_timeout(
+        ctypes.c_ulonglong(int(limit_ns)), _ptr(waited_ns), _stream(stream, dev)))

@@ -659,6 +659,7 @@ int rmsnorm_device_error(unsigned int* flags, int clear) {
     if (e == cudaSuccess) e = narrow_read_error(flags, clear != 0);
     if (e == cudaSuccess) e = wide_f16_read_error(flags, clear != 0);
     if (e == cudaSuccess) e = narrow_f16_read_error(flags, clear != 0);
+    if (e == cudaSuccess) e = selftest_read_error(flags, clear != 0);
     return cuda_status(e);
 }
 

@@ -34,7 +34,7 @@ constexpr int kMaxD = 16384;
 constexpr int kReduceWarps = 32;         // weight-gradient pass 2: warps (chunk ranges) per 32 columns
 
 // Device-side error codes (bit flags OR-ed into the library's error words).
-constexpr unsigned kErrWaitTimeout = 1u;
+constexpr unsigned kErrWaitTimeout = RMSN_DEVICE_ERR_WAIT_TIMEOUT;
 
 constexpr unsigned long long kWaitTimeoutNs = 2000000000ull;  // 2 s
 
@@ -138,8 +138,10 @@ __device__ __forceinline__ int named_bar_and(int id, int nthreads, int pred) {
 }
 
 // Bounded wait for the phase with parity `parity` to complete. Returns false if
-// kWaitTimeoutNs of global time elapsed without completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
+// `limit_ns` (the kernels use kWaitTimeoutNs) of global time elapsed without
+// completion.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
     const uint32_t addr = smem_u32(bar);
     uint32_t done = 0;
     unsigned long long t0 = 0;
@@ -153,7 +155,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity) {
         if ((it & 255u) == 0u) {
             const unsigned long long now = global_timer_ns();
             if (it == 0) t0 = now;
-            else if (now - t0 > kWaitTimeoutNs) return false;
+            else if (now - t0 > limit_ns) return false;
         }
     }
 }

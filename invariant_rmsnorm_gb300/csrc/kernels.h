@@ -111,6 +111,7 @@ int ctas_per_sm(const void* kernel, int threads, int smem_bytes);
 // Error-word access for each kernel translation unit.
 cudaError_t wide_read_error(unsigned* flags, bool clear);
 cudaError_t narrow_read_error(unsigned* flags, bool clear);
+cudaError_t selftest_read_error(unsigned* flags, bool clear);
 cudaError_t wide_f16_read_error(unsigned* flags, bool clear);
 cudaError_t narrow_f16_read_error(unsigned* flags, bool clear);
 

@@ -145,6 +145,16 @@ def test_host_step_validation_rejects_before_launch(lib):
     assert step(work=A * 16 + 16) == -2        # work not 256-byte aligned
 
 
+def test_selftest_wait_validation_rejects_before_launch(lib):
+    """The wait self-test takes a limit of 1 ns .. 1 s and an 8-byte-aligned
+    output pointer; anything else is refused before any launch."""
+    A = 1 << 20
+    st = lambda limit, out=None: lib.rmsnorm_selftest_wait_timeout(limit, out, None)
+    assert st(0) == -1 and st(1_000_000_001) == -1
+    assert st(1000, A + 4) == -2
+    assert rn.DEVICE_ERR_WAIT_TIMEOUT == 1
+
+
 def test_package_has_no_non_cuda_path():
     """The binding refuses to run without the built library (no fallback)."""
     import importlib
