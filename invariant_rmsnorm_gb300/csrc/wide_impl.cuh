@@ -15,14 +15,16 @@
 //   * Consumer thread t owns VPT 16-byte vectors of each row at slots
 //     v = k*NT + t (coalesced, conflict-free shared reads).
 //   * Fixed reduction tree (a function of D only): per-thread ascending sum
-//     over its slots and the 8 lanes of each vector, an xor-butterfly over the
+//     over its slots and the 8 elements of each vector, an xor-butterfly over the
 //     warp (offsets 16..1), then the per-warp totals added in warp order. The
 //     R rows of an iteration share one named barrier but each keeps its own
 //     tree, so a row's bits depend on nothing but the row and D: not on T, its
 //     position, the other rows, the grid or the GPU.
 //   * fp32 arithmetic with every multiply and add rounded separately (no FMA
-//     contraction), rsqrtf for the inverse RMS, round-to-nearest-even bf16 (or
-//     fp16) outputs written with 128-bit streaming stores.
+//     contraction; in some kernels the products of neighbouring elements go
+//     through the packed mul.rn.f32x2, with the same bits), rsqrtf for the
+//     inverse RMS, round-to-nearest-even bf16 (or fp16) outputs written with
+//     128-bit streaming stores.
 //   * Backward weight gradient: a CTA owns whole chunks of kWideChunkRows rows,
 //     accumulates g*x*r per column in ascending row order in registers and
 //     writes one fp32 partial row per chunk; no atomics anywhere.
@@ -465,7 +467,9 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
 // through a 4-byte cp.async, and one no-increment arrive after them makes the
 // stage's full barrier (expected count 2) wait for those copies too.
 // The products needed after the row reduction (g*w_eff, x, g*x; gated: with
-// g*silu(z) for g) are computed once before it and kept in registers.
+// g*silu(z) for g) are recomputed after it from the packed row, which stays in
+// registers (RMSN_BWD_LEAN, the default: the same bits for fewer registers);
+// with RMSN_BWD_LEAN = 0 they are computed once before it and kept.
 // ---------------------------------------------------------------------------
 template <int VPT, int MODE, int MAXT>
 __global__ void __launch_bounds__(MAXT + 32, bwd_min_blocks<VPT, MAXT, MODE>())
