@@ -22,6 +22,7 @@ from __future__ import annotations
 
 import argparse
 import hashlib
+import re
 import json
 import os
 import statistics
@@ -72,12 +73,22 @@ def peaks():
 KERNEL_SOURCES = ("api.cu", "common.cuh", "kernels.h", "reduce.cu", "wide.cu", "wide_impl.cuh")
 
 
-def source_hash():
-    h = hashlib.sha256()
+def code_text(src: str) -> str:
+    """C/C++ source without its comments and blank lines: what the compiler sees,
+    so that an edit to a comment leaves the hash below unchanged."""
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    src = re.sub(r"//[^\n]*", "", src)
+    return "\n".join(line.rstrip() for line in src.splitlines() if line.strip())
+
+
+def source_hash(read=None):
+    """Hash of the code (not the comments) of KERNEL_SOURCES; `read(name)` gives a
+    file's text (default: the working tree)."""
     csrc = os.path.join(ROOT, "invariant_rmsnorm_gb300", "csrc")
+    read = read or (lambda name: open(os.path.join(csrc, name)).read())
+    h = hashlib.sha256()
     for name in KERNEL_SOURCES:
-        with open(os.path.join(csrc, name), "rb") as f:
-            h.update(name.encode() + f.read())
+        h.update(name.encode() + code_text(read(name)).encode())
     return h.hexdigest()[:16]
 
 
