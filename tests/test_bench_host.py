@@ -1,0 +1,25 @@
+"""Host-side pieces of the benchmark: the code hash that keys the committed ncu
+traffic record, and the workload config both arms report."""
+from __future__ import annotations
+
+import bench
+
+
+def test_code_hash_ignores_comments_only():
+    src = "int f(int a) {\n  // the sum\n  return a + 1; /* one */\n}\n"
+    edited_comment = "int f(int a) {\n  // the sum, plus one\n\n  return a + 1; /* 1 */\n}\n"
+    edited_code = "int f(int a) {\n  // the sum\n  return a + 2; /* one */\n}\n"
+    assert bench.code_text(src) == bench.code_text(edited_comment)
+    assert bench.code_text(src) != bench.code_text(edited_code)
+    files = {n: src for n in bench.KERNEL_SOURCES}
+    h = bench.source_hash(lambda n: files[n])
+    files[bench.KERNEL_SOURCES[0]] = edited_comment
+    assert bench.source_hash(lambda n: files[n]) == h
+    files[bench.KERNEL_SOURCES[0]] = edited_code
+    assert bench.source_hash(lambda n: files[n]) != h
+
+
+def test_both_arms_report_the_same_config():
+    c = bench.residual_config(1)
+    assert c["T"] == 32768 and c["D"] == 4096 and c["workload"] == "rmsnorm_residual fwd+bwd"
+    assert bench.residual_config(4)["parallelism"] == "replicas x4"
