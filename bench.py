@@ -274,6 +274,12 @@ def run_ours(args):
 
     # side measurements (not part of `value`): plain and gated fwd+bwd
     extra = side_measurements(rn, synth, dev, stream) if rank == 0 else {}
+    # The dominant kernel launched back to back on its own (each launch chained
+    # to the previous one by programmatic dependent launch, as in the step):
+    # the sampled events above cost it its early launch, this does not.
+    b2b = _time_gbs(lambda: rn.rmsnorm_residual_bwd(wl.g, wl.x, wl.w, rstd, wl.g_res, dx, None, ws, False,
+                                                    stream=stream),
+                    bwd_pass1_bytes(T, D), 200, stream)
 
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
     peak, peak_kind = peaks()
@@ -304,6 +310,8 @@ def run_ours(args):
                     "serial_value": round(e2e_serial_value, 2), "serial_ms_per_step": round(e2e_ms_serial, 4)},
             "gpu_launches": 3 * args.steps,
             "clocks": clocks,
+            "bwd_pass1_back_to_back": {"us": round(b2b["ms"] * 1e3, 2), "gbs": b2b["gbs"],
+                                       "frac": round(b2b["gbs"] / peak, 4), "launches": 200},
             "cpu_baseline": cpu,
             "extra": extra,
         }
