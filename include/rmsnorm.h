@@ -310,15 +310,15 @@ int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D,
  * allocates nothing; inputs and outputs are the caller's, as in rmsnorm_bwd
  * (same arguments minus the workspace; dgamma must not be NULL).
  *   - Problems needing more scratch than the array holds, i.e. with
- *     rmsnorm_bwd_workspace_bytes(T, D) > RMSN_NOALLOC_SCRATCH_BYTES (for
- *     example T > 32768 at D = 4096), are rejected with RMSN_EWORKSPACE.
+ *     rmsnorm_bwd_workspace_bytes(T, D) > RMSN_NOALLOC_SCRATCH_BYTES, are
+ *     rejected with RMSN_EWORKSPACE. Every T up to 32768 fits at D <= 4096.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
  *   - Every call shares the one array: calls whose work overlaps on the GPU
  *     (other streams or threads, unordered) race and corrupt dgamma. Calls on
  *     one stream are safe. Leftover contents are never read.
  *   - Results are bitwise those of rmsnorm_bwd on the same inputs. */
-#define RMSN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+#define RMSN_NOALLOC_SCRATCH_BYTES ((size_t)32 << 20)
 int rmsnorm_bwd_noalloc(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int64_t ldx,
                         const float* w, const float* rstd,
                         rmsn_bf16* dx, int64_t lddx, float* dgamma,

@@ -63,8 +63,31 @@ RowCfg row_cfg(int D) {
     return c;
 }
 
+// The wide backward's weight-gradient chunk. A CTA owns whole chunks, so with
+// 32-row chunks the last round of a persistent grid can leave many CTAs idle
+// (T=32768, D=4096: 1024 chunks over 304 CTAs, 112 of them with a fourth).
+// For 2048 < D <= 7168, where the backward runs 2 CTAs per SM whatever the
+// mode, a chunk count that fills less than 90 % of its rounds of
+// kBalanceSms x 2 CTAs is evened out by shortening the chunk just enough that
+// the chunks come in whole rounds (T=32768, D=4096: 27 rows, 1214 chunks,
+// pass 1 166 -> 160 us). kBalanceSms is a constant, not the GPU's SM count:
+// the chunk, and so dgamma's bits, depend on T and D alone. Other widths and
+// well-filled rounds keep 32-row chunks (and the kernels' fixed-chunk code).
+constexpr int64_t kBalanceSms = 152;
+
+int64_t wide_chunk_rows(int64_t T, int D) {
+    constexpr int64_t c0 = kWideChunkRows;
+    if (D <= 2048 || D > 7168 || T <= 0) return c0;
+    const int64_t ctas = kBalanceSms * 2;
+    const int64_t n0 = (T + c0 - 1) / c0;
+    if (n0 <= ctas) return c0;
+    const int64_t rounds = (n0 + ctas - 1) / ctas;
+    if (10 * n0 >= 9 * rounds * ctas) return c0;
+    return (T + rounds * ctas - 1) / (rounds * ctas);  // < 32
+}
+
 int64_t num_chunks(int64_t T, int D) {
-    const int64_t c = row_cfg(D).chunk_rows;
+    const int64_t c = row_cfg(D).narrow ? row_cfg(D).chunk_rows : wide_chunk_rows(T, D);
     return (T + c - 1) / c;
 }
 
@@ -195,6 +218,7 @@ int run_fwd(int m, FwdArgs a, cudaStream_t s) {
 int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     a.inv_d_pow2 = inv_pow2(a.D);
     RowCfg c = row_cfg(a.D);
+    if (a.chunk == 0) a.chunk = static_cast<int>(wide_chunk_rows(a.T, a.D));
     // The plain backward of rows up to 2048 values runs them on at most 128
     // threads, two vectors each (a fixed function of D for this mode; measured
     // 131072 x 2048: 291 -> 282 us). The modes streaming more operands per row
@@ -212,7 +236,8 @@ int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     if (is_f16(m)) e = c.narrow ? launch_narrow_bwd_f16(m, a, c, s) : launch_wide_bwd_f16(m, a, c, s);
     else e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);
     if (e != cudaSuccess) return RMSN_ECUDA;
-    if (dgamma != nullptr) e = launch_dgamma_reduce(a.partials, num_chunks(a.T, a.D), a.D, dgamma, s);
+    const int64_t nchunks = c.narrow ? num_chunks(a.T, a.D) : (a.T + a.chunk - 1) / a.chunk;
+    if (dgamma != nullptr) e = launch_dgamma_reduce(a.partials, nchunks, a.D, dgamma, s);
     return cuda_status(e);
 }
 
@@ -425,6 +450,36 @@ int rmsnorm_gated_bwd_recompute_impl(int flags, const rmsn_act16* g, int64_t ldg
 }
 
 }  // namespace
+
+// The rmsnorm_residual backward of T rows with the weight-gradient chunk of a
+// chunk_T-row problem (for the host-buffer step, whose slabs must write the
+// chunk partials of the whole problem). Only pass 1 runs.
+int rmsn::residual_bwd_chunk_of(int64_t chunk_T, const uint16_t* g, int64_t ldg, const uint16_t* x, int64_t ldx,
+                                const float* w, const float* rstd, const uint16_t* g_res, int64_t ldgr, uint16_t* dx,
+                                int64_t lddx, void* ws, size_t ws_bytes, int64_t T, int64_t D,
+                                int zero_centered_gamma, int dtype, cudaStream_t stream) {
+    int flags = 0;
+    RMSN_TRY(dtype_flags(dtype, &flags));
+    RMSN_TRY(check_shape(T, D));
+    if (T == 0) return RMSN_OK;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    if (g_res) RMSN_TRY(check_act(g_res, ldgr, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    const RowCfg c = row_cfg(static_cast<int>(D));
+    const int64_t chunk = c.narrow ? c.chunk_rows : wide_chunk_rows(chunk_T, static_cast<int>(D));
+    const size_t need = static_cast<size_t>((T + chunk - 1) / chunk) * static_cast<size_t>(D) * 4u;
+    if (ws == nullptr || ws_bytes < need) return RMSN_EWORKSPACE;
+    if (!aligned16(ws)) return RMSN_EALIGN;
+    BwdArgs a{};
+    a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.gres = g_res; a.ldgr = ldgr; a.w = w; a.rstd = rstd;
+    a.dx = dx; a.lddx = lddx; a.partials = static_cast<float*>(ws);
+    a.T = T; a.D = static_cast<int>(D); a.zc = zero_centered_gamma ? 1 : 0;
+    a.chunk = c.narrow ? 0 : static_cast<int>(chunk);
+    return run_bwd((g_res ? kResidual : kPlain) | flags, a, nullptr, stream);
+}
 
 // ---------------------------------------------------------------------------
 // Entry points

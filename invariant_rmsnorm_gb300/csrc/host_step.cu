@@ -52,11 +52,18 @@ struct WorkLayout {
     size_t w = 0, dgamma = 0, partials = 0, slot0 = 0, slot_bytes = 0, total = 0;
 };
 
+// Rows per weight-gradient chunk of the whole T-row problem: every slab starts
+// on a chunk boundary and its backward writes the whole problem's chunks.
+int64_t step_chunk_rows(int64_t T, int64_t D) {
+    const RowCfg c = row_cfg(static_cast<int>(D));
+    return c.narrow ? c.chunk_rows : wide_chunk_rows(T, static_cast<int>(D));
+}
+
 // Slab rows: the request (0 = default), rounded up to whole chunks and capped
 // at the chunk-rounded T.
 WorkLayout layout(int64_t T, int64_t D, int64_t slab_rows) {
     WorkLayout L{};
-    const int64_t chunk = row_cfg(static_cast<int>(D)).chunk_rows;
+    const int64_t chunk = step_chunk_rows(T, D);
     int64_t s = slab_rows > 0 ? slab_rows : kDefaultSlabRows;
     s = (s + chunk - 1) / chunk * chunk;
     const int64_t t_chunks = (T + chunk - 1) / chunk * chunk;
@@ -165,7 +172,7 @@ extern "C" int rmsnorm_residual_step_host(const rmsn_act16* x, const rmsn_act16*
     float* d_dgamma = reinterpret_cast<float*>(base + L.dgamma);
     unsigned char* d_partials = base + L.partials;
     const size_t partials_bytes = rmsnorm_bwd_workspace_bytes(T, D);
-    const int64_t chunk = row_cfg(static_cast<int>(D)).chunk_rows;
+    const int64_t chunk = step_chunk_rows(T, D);
     const size_t row_bytes = static_cast<size_t>(D) * 2u;
     const size_t chunk_partial_bytes = static_cast<size_t>(D) * 4u;
     cudaStream_t s = reinterpret_cast<cudaStream_t>(stream);
@@ -212,9 +219,9 @@ extern "C" int rmsnorm_residual_step_host(const rmsn_act16* x, const rmsn_act16*
         RMSN_STEP_TRY(rmsnorm_residual_fwd_ex(s_x, D, d_w, s_y, D, s_rstd, s_xc, D, rows, D, eps,
                                               zero_centered_gamma, dtype, stream));
         const size_t p_off = static_cast<size_t>(a / chunk) * chunk_partial_bytes;
-        RMSN_STEP_TRY(rmsnorm_residual_bwd_ex(s_g, D, s_x, D, d_w, s_rstd, g_res != nullptr ? s_gr : nullptr, D,
-                                              s_dx, D, nullptr, d_partials + p_off, partials_bytes - p_off,
-                                              rows, D, zero_centered_gamma, dtype, stream));
+        RMSN_STEP_TRY(residual_bwd_chunk_of(T, s_g, D, s_x, D, d_w, s_rstd, g_res != nullptr ? s_gr : nullptr, D,
+                                            s_dx, D, d_partials + p_off, partials_bytes - p_off, rows, D,
+                                            zero_centered_gamma, dtype, s));
         RMSN_STEP_CUDA(cudaEventRecord(c->computed[slot], s));
 
         // Outputs out.

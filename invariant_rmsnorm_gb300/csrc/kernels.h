@@ -70,6 +70,7 @@ struct BwdArgs {
     uint16_t* y; int64_t ldy;           // optional: the forward output, recomputed (null = skip)
     int64_t T; int D; int zc;
     float inv_d_pow2;                   // 1/D if D is a power of two, else 0
+    int chunk;                          // wide path: rows per weight-gradient chunk (0: wide_chunk_rows(T, D))
 };
 
 // Row-shape configuration: a pure function of D.
@@ -88,6 +89,16 @@ RowCfg row_cfg(int D);
 int narrow_chunk_rows_for_group(int G);
 int narrow_stage_rows_for_group(int G);
 int64_t num_chunks(int64_t T, int D);
+// Rows per weight-gradient chunk of the wide backward (D > 256) for T rows:
+// a function of T and D only (see api.cu).
+int64_t wide_chunk_rows(int64_t T, int D);
+// The rmsnorm_residual backward with the weight-gradient chunk of `chunk_T`
+// rows' problem instead of its own T (so that a slice of rows writes the same
+// chunk partials as the whole problem would); otherwise rmsnorm_residual_bwd_ex.
+int residual_bwd_chunk_of(int64_t chunk_T, const uint16_t* g, int64_t ldg, const uint16_t* x, int64_t ldx,
+                          const float* w, const float* rstd, const uint16_t* g_res, int64_t ldgr, uint16_t* dx,
+                          int64_t lddx, void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma,
+                          int dtype, cudaStream_t stream);
 
 // Launchers (return the launch's cudaError_t; arguments already validated).
 // `m` is a Mode with its variant flags. The bf16 variants are instantiated in

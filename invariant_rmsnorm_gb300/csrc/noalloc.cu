@@ -8,7 +8,7 @@
 // serves them: it keeps the scratch in a fixed array that is part of this
 // library's device image, so the call itself allocates nothing.
 //
-// The array is RMSN_NOALLOC_SCRATCH_BYTES (16 MiB) on every GPU where the
+// The array is RMSN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU where the
 // library's device code is loaded, held until the process exits. Its device
 // address is looked up once per device, on the first call made with that
 // device current (so that first call should come before any stream capture).

@@ -471,17 +471,21 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
 // registers (RMSN_BWD_LEAN, the default: the same bits for fewer registers);
 // with RMSN_BWD_LEAN = 0 they are computed once before it and kept.
 // ---------------------------------------------------------------------------
-template <int VPT, int MODE, int MAXT>
+template <int VPT, int MODE, int MAXT, bool VC = false>
 __global__ void __launch_bounds__(MAXT + 32, bwd_min_blocks<VPT, MAXT, MODE>())
 wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr int M = base_mode(MODE);
     constexpr bool F16 = is_f16(MODE);
     constexpr bool SIG = is_sigmoid_gate(MODE);
     constexpr int NIN = bwd_inputs(MODE);
-    constexpr int C = kWideChunkRows;
     constexpr int R = bwd_rows<VPT, MAXT>();
     constexpr int NWMAX = MAXT / 32;
-    static_assert(C % R == 0, "rows per iteration must divide the chunk");
+    // Rows per weight-gradient chunk: kWideChunkRows, or with VC the chunk the
+    // host chose for T (a.chunk, which R divides); VC kernels step through
+    // their rows without dividing by it.
+    constexpr int C0 = kWideChunkRows;
+    static_assert(C0 % R == 0, "rows per iteration must divide the chunk");
+    const int C = VC ? a.chunk : C0;
     // Register diet of the widest rows (VPT 4 on 512 threads, D > 8192, where
     // the launch allows about 96 registers): HOLD re-reads the staged operands
     // after the row reduction instead of keeping them packed in registers (the
@@ -531,8 +535,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         n_my = static_cast<int>((cnt - 1) * C + last_rows);
     }
     const int n_it = (n_my + R - 1) / R;
-    // k-th row of this CTA (C is a power of two: shifts, no divisions).
-    auto row_of = [&](int k) -> int64_t { return (cta + static_cast<int64_t>(k / C) * G) * C + (k % C); };
+    // k-th row of this CTA with the fixed chunk (C0 is a power of two: shifts).
+    auto row_of = [&](int k) -> int64_t { return (cta + static_cast<int64_t>(k / C0) * G) * C0 + (k % C0); };
 
     if (tid == 0) {
         for (int s = 0; s < S; ++s) {
@@ -550,20 +554,31 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             // Operands after g and x: residual g_res; gated z; fused add res, then g_res.
             const uint16_t* third = (M == kResidual) ? a.gres : (M == kGated ? a.z : a.res);
             const int64_t ld_third = (M == kResidual) ? a.ldgr : (M == kGated ? a.ldz : a.ldres);
+            // Iteration i's first row, stepped like the consumers' (no division):
+            // iterations come in order, R rows each, never straddling a chunk.
+            int64_t row0 = cta * C;
+            int po = 0;
             produce(full, empty, S, n_it, [&](int i, int s) {
                 unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
                 const int nvalid = min(n_my - i * R, R);
                 mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nvalid) * NIN * row_bytes);
-                for (int r = 0; r < nvalid; ++r) cp_async4(&rs[s * R + r], a.rstd + row_of(i * R + r));
+                for (int r = 0; r < nvalid; ++r)
+                    cp_async4(&rs[s * R + r], a.rstd + (VC ? row0 + r : row_of(i * R + r)));
                 cp_async_arrive_noinc(&full[s]);
                 for (int r = 0; r < nvalid; ++r) {
-                    const int64_t row = row_of(i * R + r);
+                    const int64_t row = VC ? row0 + r : row_of(i * R + r);
                     unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
                     bulk_g2s(dst, a.g + row * a.ldg, row_bytes, &full[s], pol);
                     bulk_g2s(dst + row_bytes, a.x + row * a.ldx, row_bytes, &full[s], pol);
                     if (NIN >= 3)
                         bulk_g2s(dst + 2 * row_bytes, third + row * ld_third, row_bytes, &full[s], pol);
                     if (NIN == 4) bulk_g2s(dst + 3 * row_bytes, a.gres + row * a.ldgr, row_bytes, &full[s], pol);
+                }
+                row0 += R;
+                po += R;
+                if (po == C) {  // next chunk of this CTA: G chunks further on
+                    po = 0;
+                    row0 += (G - 1) * C;
                 }
             });
         }
@@ -580,6 +595,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
 
     int s = 0;
     uint32_t ph = 0;
+    int kc = 0, ko = 0;  // this iteration's first row: chunk ordinal kc, offset ko within it
     for (int i = 0; i < n_it; ++i) {
         const bool ok = mbar_wait(&full[s], ph);
         const unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
@@ -682,7 +698,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                 const float r1 = rr[r];
                 const float s_tot = block_total<NWMAX>(rb + r * 32, nw);
                 const float coef = fmul(div_by_d(fmul(fmul(r1, r1), r1), D, a.inv_d_pow2), s_tot);
-                const int64_t row = row_of(i * R + r);
+                const int64_t row = VC ? (cta + static_cast<int64_t>(kc) * G) * C + ko + r : row_of(i * R + r);
                 uint16_t* dxrow = a.dx + row * a.lddx;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
@@ -817,8 +833,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         }
         // End of a chunk: write its partial row and restart the accumulators.
         const int k_last = i * R + nvalid - 1;
-        if ((k_last % C) == C - 1 || k_last == n_my - 1) {
-            const int64_t chunk = cta + static_cast<int64_t>(k_last / C) * G;
+        if ((VC ? ko + nvalid == C : (k_last % C0) == C0 - 1) || k_last == n_my - 1) {
+            const int64_t chunk = cta + static_cast<int64_t>(VC ? kc : k_last / C0) * G;
             float* prow = a.partials + chunk * D;
             // Partials are re-read by pass 2 right away: keep them in L2.
             const uint64_t keep = policy_evict_last();
@@ -832,6 +848,11 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
 #pragma unroll
                 for (int e = 0; e < 8; ++e) acc[j][e] = 0.0f;
             }
+        }
+        ko += R;
+        if (ko == C) {
+            ko = 0;
+            ++kc;
         }
     }
     pdl_release();
@@ -875,7 +896,7 @@ cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
     return launch_kernel(wide_fwd_kernel<VPT, MODE, MAXT>, static_cast<unsigned>(grid), threads, smem, st, a, S);
 }
 
-template <int VPT, int MODE, int MAXT>
+template <int VPT, int MODE, int MAXT, bool VC = false>
 cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     constexpr int NIN = bwd_inputs(MODE);
     constexpr int R = bwd_rows<VPT, MAXT>();
@@ -885,14 +906,14 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const size_t smem = S * (stage + 16 + 4 * R) + fixed;
     if (smem > static_cast<size_t>(kMaxSmemPerCta)) return cudaErrorInvalidConfiguration;
     const int threads = c.bwd_threads + 32;
-    const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT>);
+    const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT, VC>);
     cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT, MODE>());
     if (occ < 1) return cudaErrorInvalidConfiguration;
-    const int64_t nchunks = (a.T + kWideChunkRows - 1) / kWideChunkRows;
+    const int64_t nchunks = (a.T + a.chunk - 1) / a.chunk;
     const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
-    return launch_kernel(wide_bwd_kernel<VPT, MODE, MAXT>, static_cast<unsigned>(grid), threads, smem, st, a, S);
+    return launch_kernel(wide_bwd_kernel<VPT, MODE, MAXT, VC>, static_cast<unsigned>(grid), threads, smem, st, a, S);
 }
 
 template <int MODE>
@@ -909,16 +930,23 @@ cudaError_t fwd_dispatch(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
 template <int MODE>
 cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     const bool big = c.bwd_threads > 256;
+    // A chunk other than kWideChunkRows (2048 < D <= 7168 only) runs the
+    // stepping instantiation of the two kernels those widths use.
+    const bool vc = a.chunk != kWideChunkRows;
     switch (c.bwd_vpt) {
-        case 1: return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
+        case 1:
+            if (vc) return cudaErrorInvalidValue;
+            return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
         case 2:
-            if (big) return bwd_t<2, MODE, 512>(a, c, st);
-            if (c.bwd_threads <= 128) return bwd_t<2, MODE, 128>(a, c, st);  // rows of 2 vectors a thread on <= 128 threads
-            return bwd_t<2, MODE, 256>(a, c, st);
+            if (big) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 512>(a, c, st);
+            if (c.bwd_threads <= 128)  // rows of 2 vectors a thread on <= 128 threads
+                return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 128>(a, c, st);
+            return vc ? bwd_t<2, MODE, 256, true>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
         case 4:
-            if (big) return bwd_t<4, MODE, 512>(a, c, st);
-            if (RMSN_BWD_V4_224 && c.bwd_threads <= 224) return bwd_t<4, MODE, 224>(a, c, st);
-            return bwd_t<4, MODE, 256>(a, c, st);
+            if (big) return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 512>(a, c, st);
+            if (RMSN_BWD_V4_224 && c.bwd_threads <= 224)
+                return vc ? bwd_t<4, MODE, 224, true>(a, c, st) : bwd_t<4, MODE, 224>(a, c, st);
+            return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 256>(a, c, st);
         default: return cudaErrorInvalidValue;
     }
 }

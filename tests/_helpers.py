@@ -197,8 +197,26 @@ def assert_dgamma_parity(name, got, ref, abs_sum, chunk_rows: int, nchunks: int)
     return int(np.count_nonzero(m2 & ~m1))
 
 
-WIDE_CHUNK_ROWS = 32    # weight-gradient chunk of the wide path (D > 256)
+WIDE_CHUNK_ROWS = 32    # longest weight-gradient chunk of the wide path (D > 256)
 PASS2_RANGES = 32       # pass-2 ranges of contiguous chunks
+BALANCE_SMS = 152       # the constant the wide chunk rule balances for
+
+
+def wide_chunk_rows(T: int, D: int) -> int:
+    """The wide backward's chunk rule: 32 rows, except for 2048 < D <= 7168
+    when 32-row chunks fill less than 90 % of their rounds of 152 x 2 CTAs;
+    then 32 rows shortened just enough that the chunks come in whole rounds."""
+    c0 = WIDE_CHUNK_ROWS
+    if D <= 2048 or D > 7168 or T <= 0:
+        return c0
+    ctas = BALANCE_SMS * 2
+    n0 = -(-T // c0)
+    if n0 <= ctas:
+        return c0
+    rounds = -(-n0 // ctas)
+    if 10 * n0 >= 9 * rounds * ctas:
+        return c0
+    return -(-T // (rounds * ctas))
 
 
 def _pass2(partials):
@@ -228,8 +246,8 @@ def dgamma_model(g, h, r, fused: bool = False):
     multiply and add rounded to fp32, summed per chunk in the order the path
     fixes, then the chunk partials through the pass-2 tree (32 contiguous
     ranges of ceil(n/32) chunks in ascending order, the range totals in order).
-    g, h [T, D] and r [T] are float32 and exact. D > 256 (wide path): 32-row
-    chunks, rows in ascending order. D <= 256 (narrow path): G = next power of
+    g, h [T, D] and r [T] are float32 and exact. D > 256 (wide path): chunks of
+    wide_chunk_rows(T, D) rows, rows in ascending order. D <= 256 (narrow path): G = next power of
     two of D/8 lanes per row, P = 256/G rows per pass, stages of RS = 32 rows
     (P if larger; 32 when G = 32), chunks of max(RS, 128) rows; lane group q
     adds the rows chunk + s*RS + p*P + q, stage by stage and pass by pass, and
@@ -238,11 +256,12 @@ def dgamma_model(g, h, r, fused: bool = False):
     rounded once), the rounding the kernels must not do."""
     T, D = g.shape
     if D > 256:
-        nch = -(-T // WIDE_CHUNK_ROWS)
+        C = wide_chunk_rows(T, D)
+        nch = -(-T // C)
         partials = np.zeros((nch, D), np.float32)
         for c in range(nch):
             acc = np.zeros(D, np.float32)
-            for t in range(c * WIDE_CHUNK_ROWS, min(T, (c + 1) * WIDE_CHUNK_ROWS)):
+            for t in range(c * C, min(T, (c + 1) * C)):
                 acc = _accumulate(acc, g[t] * h[t], r[t], fused)
             partials[c] = acc
         return _pass2(partials)

@@ -71,6 +71,7 @@ def _assert_same(host, dev, name):
     (777, 264, 32, torch.bfloat16),        # wide, one chunk per slab, ragged tail
     (4097, 4096, 0, torch.bfloat16),       # default slab, one-row last slab
     (3000, 4096, 512, torch.float16),
+    (10000, 4096, 1000, torch.bfloat16),   # 17-row chunks: slabs of 1003 rows
     (257, 16384, 96, torch.bfloat16),      # widest rows
 ])
 def test_host_step_matches_device_entry_points(T, D, slab, dtype):
