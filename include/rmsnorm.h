@@ -96,8 +96,17 @@ int rmsnorm_fwd(const rmsn_bf16* x, int64_t ldx, const float* w,
                 int64_t T, int64_t D, float eps, int zero_centered_gamma, rmsn_stream stream);
 
 /* Bytes of workspace the backward entry points need for T rows of width D
- * (0 for T == 0; also 0 for an unsupported D). */
+ * (0 for T == 0; also 0 for an unsupported D). Not monotone in T: at some
+ * widths the weight-gradient chunk is shortened so that chunks fill whole
+ * rounds of the grid, and a larger T can then need fewer bytes than a smaller
+ * one (D = 4096: T = 20000 needs more than T = 27360). To size one buffer for
+ * every T up to a maximum, use rmsnorm_bwd_workspace_bytes_max. */
 size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t D);
+
+/* The largest rmsnorm_bwd_workspace_bytes(T, D) over 0 <= T <= T_max: one
+ * buffer of this many bytes serves every such T (0 for T_max <= 0 or an
+ * unsupported D). */
+size_t rmsnorm_bwd_workspace_bytes_max(int64_t T_max, int64_t D);
 
 /* Backward, plain or zero-centred ([Megatron] item 2; [Residual] Backward).
  *   g [T][ldg] (dL/dy) in, x [T][ldx] in, w [D] in, rstd [T] in (the forward's),

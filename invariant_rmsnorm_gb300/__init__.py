@@ -36,7 +36,7 @@ __all__ = [
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
     "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex", "DTYPE_CODES", "GATE_CODES",
     "rmsnorm_residual_step_host", "rmsnorm_residual_step_host_work_bytes", "rmsnorm_selftest_wait_timeout",
-    "DEVICE_ERR_WAIT_TIMEOUT",
+    "DEVICE_ERR_WAIT_TIMEOUT", "rmsnorm_bwd_workspace_bytes_max",
 ]
 
 EXPORTED_SYMBOLS = (
@@ -49,6 +49,7 @@ EXPORTED_SYMBOLS = (
     "rmsnorm_gated_fwd_ex", "rmsnorm_gated_bwd_ex", "rmsnorm_fused_add_fwd_ex", "rmsnorm_fused_add_bwd_ex",
     "rmsnorm_bwd_recompute_ex", "rmsnorm_gated_bwd_recompute_ex",
     "rmsnorm_residual_step_host_work_bytes", "rmsnorm_residual_step_host", "rmsnorm_selftest_wait_timeout",
+    "rmsnorm_bwd_workspace_bytes_max",
 )
 
 # RMSN_DEVICE_ERR_WAIT_TIMEOUT of include/rmsnorm.h: the flag a wait that ran out of time raises
@@ -88,6 +89,7 @@ _SIGS = {
                                            _P, _SZ, _I64, _I64, _INT, _P]),
 }
 _SIGS["rmsnorm_residual_step_host_work_bytes"] = (_SZ, [_I64, _I64, _I64])
+_SIGS["rmsnorm_bwd_workspace_bytes_max"] = (_SZ, [_I64, _I64])
 _SIGS["rmsnorm_selftest_wait_timeout"] = (_INT, [ctypes.c_ulonglong, _P, _P])
 _SIGS["rmsnorm_residual_step_host"] = (_INT, [_P] * 9 + [_I64, _I64, _F, _INT, _INT, _I64, _P, _SZ, _P])
 # Each *_ex call: the unsuffixed signature with `int dtype` (gated: `int gate, int dtype`) before the stream.
@@ -197,6 +199,12 @@ def rmsnorm_bwd_workspace_bytes(T: int, D: int) -> int:
 
 
 workspace_bytes = rmsnorm_bwd_workspace_bytes
+
+
+def rmsnorm_bwd_workspace_bytes_max(T_max: int, D: int) -> int:
+    """Bytes of one workspace that serves every T up to T_max (the per-T size is
+    not monotone in T at some widths)."""
+    return int(load().rmsnorm_bwd_workspace_bytes_max(int(T_max), int(D)))
 
 
 def rmsnorm_fwd(x, w, y, rstd, eps: float = 1e-6, zero_centered_gamma: bool = False, stream=None):

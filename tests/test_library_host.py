@@ -109,6 +109,22 @@ def test_ex_options_are_validated_on_the_host(lib):
     assert lib.rmsnorm_residual_fwd_ex(0, 0, 0, 0, 0, 0, 0, 0, 0, 128, 1e-6, 0, 1, None) == 0  # T = 0
 
 
+def test_workspace_size_is_not_monotone_and_the_max_query_covers_it(lib):
+    """The chunk rule makes the per-T size non-monotone at 2048 < D <= 7168; the
+    max query bounds every T up to its argument and equals the per-T size where
+    the size grows with T."""
+    q, qmax = rn.rmsnorm_bwd_workspace_bytes, rn.rmsnorm_bwd_workspace_bytes_max
+    assert q(20000, 4096) > q(27360, 4096)
+    for D in (4096, 7168):
+        sizes = [q(t, D) for t in range(1, 40001, 7)]
+        m = qmax(40000, D)
+        assert m >= max(sizes) and m >= q(40000, D)
+        assert m == max(q(t, D) for t in range(1, 40001))
+    for T, D in ((100000, 2048), (70000, 128), (50000, 8192), (200000, 4096)):
+        assert qmax(T, D) == q(T, D)  # the size grows with T here
+    assert qmax(0, 4096) == 0 and qmax(100, 7) == 0
+
+
 @pytest.mark.parametrize("T,D", [(1, 128), (100, 64), (32768, 4096), (4097, 4096), (70000, 8)])
 def test_host_step_work_query(lib, T, D):
     """The host-buffer step's device work buffer: the weight-gradient partials
