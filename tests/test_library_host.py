@@ -109,6 +109,21 @@ def test_ex_options_are_validated_on_the_host(lib):
     assert lib.rmsnorm_residual_fwd_ex(0, 0, 0, 0, 0, 0, 0, 0, 0, 128, 1e-6, 0, 1, None) == 0  # T = 0
 
 
+def test_library_chunk_rule_matches_the_test_model(lib):
+    """The workspace query reveals the library's weight-gradient chunk count for
+    any T; it must be the count of the chunk rule the bit-for-bit tests model
+    (tests/_helpers.py wide_chunk_rows), over widths inside and outside the band
+    where chunks are shortened."""
+    from tests._helpers import wide_chunk_rows
+    rng = __import__("numpy").random.default_rng(4)
+    Ts = sorted(set([1, 31, 32, 33, 9728, 9729, 10000, 19456, 19457, 20000, 27360, 32768, 38912, 87552,
+                     87553, 97280, 131072, 262144] + [int(t) for t in rng.integers(1, 300000, 200)]))
+    for D in (264, 2048, 2056, 4096, 7168, 7176, 8192, 16384):
+        for T in Ts:
+            n = rn.rmsnorm_bwd_workspace_bytes(T, D) // (4 * D)
+            assert n == -(-T // wide_chunk_rows(T, D)), (T, D, n)
+
+
 def test_workspace_size_is_not_monotone_and_the_max_query_covers_it(lib):
     """The chunk rule makes the per-T size non-monotone at 2048 < D <= 7168; the
     max query bounds every T up to its argument and equals the per-T size where
