@@ -276,8 +276,8 @@ void orc_gated_bwd(int64_t T, int64_t D, const double* g, const double* x, const
 }
 
 /* ------------------------------------------------------------------------ */
-/* Fused add + RMSNorm (vLLM fused_add_rms_norm, the decoder-norm path of     */
-/* [ZC-norm], "Only layer 0's input norm takes the no-residual path"): the   */
+/* Fused add + RMSNorm (vLLM fused_add_rms_norm, which [ZC-norm] names as    */
+/* the path of every decoder norm except layer 0's input norm): the          */
 /* norm is applied to the fp32 sum h = x + res, which is also returned       */
 /* rounded to the activation format as the new residual stream.             */
 /*   h = fl32(x + res);  res_out = act(h);  rstd, y as the plain forward on h  */
