@@ -22,9 +22,10 @@
  * Batch invariance: every row is reduced by a fixed tree whose shape depends on
  * D alone, so y[t], rstd[t] and dx[t] are bitwise independent of T, of the row's
  * position, of the other rows and of the GPU's SM count. dgamma is a sum over
- * rows; it is computed with no atomics, in fixed-size row chunks (pass 1) whose
- * partial sums are added in a fixed order (pass 2), so it is bitwise identical
- * from run to run and across GPUs with different SM counts.
+ * rows; it is computed with no atomics, in row chunks whose size depends on T
+ * and D alone (pass 1), whose partial sums are added in a fixed order (pass 2),
+ * so it is bitwise identical from run to run and across GPUs with different
+ * SM counts.
  *
  * Common conventions for every entry point:
  *   - Activations (x, z, g, g_res, y, dx, dz, x_copy) are bf16 (fp16 as an
@@ -356,8 +357,10 @@ int rmsnorm_bwd_noalloc(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, int
  *     a [slab] fp32 buffer each), w, dgamma and the weight-gradient partials of
  *     all T rows. Too small or NULL: RMSN_EWORKSPACE; misaligned: RMSN_EALIGN.
  *     Calls that overlap on the GPU must not share one work buffer.
- *   - slab_rows: rows per slab, rounded up to the weight-gradient chunk (32
- *     rows for D > 256) and capped at T; 0 takes the default, 4096.
+ *   - slab_rows: rows per slab, rounded up to a multiple of the weight-gradient
+ *     chunk of the whole problem (for D > 256: 32 rows, or fewer at some T for
+ *     2048 < D <= 7168; for D <= 256: 128 rows or more) and capped at T; 0
+ *     takes the default, 4096.
  *   - The kernels run on `stream`; the copies run on two copy streams per
  *     device that the library creates on the first call made with that device
  *     current (make that first call outside any stream capture) and keeps
