@@ -65,6 +65,7 @@ WorkLayout layout(int64_t T, int64_t D, int64_t slab_rows) {
     WorkLayout L{};
     const int64_t chunk = step_chunk_rows(T, D);
     int64_t s = slab_rows > 0 ? slab_rows : kDefaultSlabRows;
+    if (s > T) s = T;  // first, so that the rounding below cannot overflow
     s = (s + chunk - 1) / chunk * chunk;
     const int64_t t_chunks = (T + chunk - 1) / chunk * chunk;
     if (s > t_chunks) s = t_chunks;

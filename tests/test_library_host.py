@@ -154,6 +154,7 @@ def test_host_step_work_query(lib, T, D):
     assert b >= part + slots * (6 * slab * D * 2 + slab * 4)
     assert b < part + slots * (6 * (slab + 256) * D * 2 + (slab + 256) * 4) + 8 * D + 4096
     assert q(T, D, 10 ** 9) == q(T, D, T)                 # capped at T
+    assert q(T, D, 2 ** 63 - 1) == q(T, D, T)             # no overflow in the rounding
     assert q(T, D, 1) <= b                                # one chunk per slab
     assert q(0, D) == 0 and q(T, 7) == 0 and q(T, D, -1) == 0
 
