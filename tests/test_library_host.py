@@ -116,7 +116,7 @@ def test_library_chunk_rule_matches_the_test_model(lib):
     where chunks are shortened."""
     from tests._helpers import wide_chunk_rows
     rng = __import__("numpy").random.default_rng(4)
-    Ts = sorted(set([1, 31, 32, 33, 9728, 9729, 10000, 19456, 19457, 20000, 27360, 32768, 38912, 87552,
+    Ts = sorted(set([1, 31, 32, 33, 9728, 9729, 10000, 19456, 19457, 20000, 27360, 32768, 38912, 78784, 78785, 87552,
                      87553, 97280, 131072, 262144] + [int(t) for t in rng.integers(1, 300000, 200)]))
     for D in (264, 2048, 2056, 4096, 7168, 7176, 8192, 16384):
         for T in Ts:
