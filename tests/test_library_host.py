@@ -42,6 +42,45 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
+def _declarations():
+    """(return type, name, [parameter types]) of every entry point in include/*.h."""
+    out = []
+    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
+        txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        txt = "\n".join(l for l in txt.split("\n") if not l.strip().startswith("#"))
+        for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\b(rmsnorm_\w+)\s*\(([^)]*)\)\s*;", txt):
+            types = [re.sub(r"\b\w+$", "", q.strip()).strip() for q in params.split(",") if q.strip()]
+            out.append((" ".join(ret.split()).replace(" *", "*"), name, types))
+    return out
+
+
+_SCALARS = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "float": ctypes.c_float, "size_t": ctypes.c_size_t,
+            "unsigned long long": ctypes.c_ulonglong, "rmsn_stream": ctypes.c_void_p}
+
+
+def _matches(c_type, ct):
+    if c_type.endswith("*"):
+        return ct in (ctypes.c_void_p, ctypes.c_char_p) or issubclass(ct, ctypes._Pointer)
+    return ct is _SCALARS[c_type]
+
+
+def test_binding_signatures_match_the_header(lib):
+    """Every ctypes prototype of the binding has the header's parameter count
+    and, position by position, a type of the same kind and width (a pointer, or
+    the same integer / float type), and the same return type: a mismatch would
+    pass garbage through the C ABI without any error."""
+    decls = _declarations()
+    assert {n for _, n, _ in decls} == set(rn.EXPORTED_SYMBOLS)
+    for ret, name, types in decls:
+        res, args = rn._SIGS[name]
+        assert len(args) == len(types), (name, len(args), len(types))
+        for i, (c_type, ct) in enumerate(zip(types, args)):
+            assert _matches(c_type, ct), (name, i, c_type, ct)
+        assert _matches(ret, res), (name, ret, res)
+        fn = getattr(lib, name)
+        assert fn.restype is res and list(fn.argtypes) == list(args), name
+
+
 def test_status_strings(lib):
     for st in (0, -1, -2, -3, -4, -5):
         assert rn.rmsnorm_status_string(st).startswith("RMSN_")
