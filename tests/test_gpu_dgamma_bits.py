@@ -4,8 +4,9 @@ model of its stated arithmetic.
 Per RL-Kernel pull request 414 "[DSv4][P1-5] rmsnorm_residual" (Implementation:
 ascending fp32 reductions, every multiply and add rounded on its own, no
 atomics), dgamma_j is built from the products ((g_tj * x_tj) * r_t), each
-rounded to fp32, added in ascending row order within each 32-row chunk (pass 1),
-(wide path; the narrow path's order is described below), and the chunk
+rounded to fp32, added in ascending row order within each chunk (pass 1; wide
+path: chunks of wide_chunk_rows(T, D) rows, 32 or, at some T for
+2048 < D <= 7168, fewer; the narrow path's order is described below), and the chunk
 partials added by the fixed pass-2 tree: 32 contiguous ranges of
 ceil(n / 32) chunks, each summed in ascending order, then the 32 range totals
 in order. Every operand here is exact in fp32 (bf16 or fp16 activations, the
