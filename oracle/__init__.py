@@ -34,6 +34,7 @@ in ``tests/test_oracle_pins.py``.
 from __future__ import annotations
 
 import ctypes
+import os
 import threading
 
 import numpy as np
@@ -59,7 +60,9 @@ def _load():
     global _lib
     with _lock:
         if _lib is None:
-            lib = ctypes.CDLL(_build.build())
+            # RMSN_ORACLE_LIB names another build of the oracle source: the
+            # planted-mistake test loads altered copies through it.
+            lib = ctypes.CDLL(os.environ.get("RMSN_ORACLE_LIB") or _build.build())
             lib.orc_num_threads.restype = _INT
             lib.orc_round_bf16.restype = ctypes.c_double
             lib.orc_round_bf16.argtypes = [ctypes.c_double]

@@ -320,8 +320,8 @@ void orc_fused_add_bwd(int64_t T, int64_t D, const double* g, const double* x, c
 /* ------------------------------------------------------------------------ */
 /* Gated norm, HF/transformers convention, forward only ([ZC-norm]: the two  */
 /* upstreams round the gated norm differently; the vLLM one multiplies by    */
-/* the weight in fp32, and with fp32 inputs the two agree bitwise because    */
-/* "the cast" is then a no-op). Reading: the normalised value is cast to the */
+/* the weight in fp32, and with fp32 inputs the two agree bitwise, since the */
+/* cast then changes nothing). Reading: the normalised value is cast to the  */
 /* activation dtype (bf16) and the weight multiply happens in that dtype:    */
 /*   n = bf16(fl32(x r));  t = bf16(fl32(bf16(w_eff) n));  y = bf16(t silu(z)) */
 /* In unrounded mode every cast is the identity, so the function equals the  */

@@ -74,6 +74,19 @@ def f16_round_bruteforce(v) -> float:
     return _round_bruteforce(v, _f16_table())
 
 
+def fp32_round_exact(v) -> float:
+    """Nearest fp32 value to the exact rational ``v`` (ties to the even bit
+    pattern), by exact comparison of the candidates' distances. The double
+    nearest to v, cast to fp32, is the answer or a neighbour of it (a double
+    rounding errs by at most one step), so those three are the candidates."""
+    v = Fraction(v)
+    f = np.float32(float(v))
+    cands = [c for c in (f, np.nextafter(f, np.float32(np.inf)), np.nextafter(f, np.float32(-np.inf)))
+             if np.isfinite(c)]
+    return float(min(cands, key=lambda c: (abs(Fraction(float(c)) - v),
+                                           int(np.array(c, np.float32).view(np.uint32)) & 1)))
+
+
 def _round_bruteforce(v, tab) -> float:
     v = Fraction(v)
     a = abs(v)

@@ -25,7 +25,7 @@ import pytest
 import torch
 
 import oracle
-from tests._helpers import bf16_round_bruteforce, fd_grad
+from tests._helpers import bf16_round_bruteforce, fd_grad, fp32_round_exact
 
 GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
 RNG = np.random.default_rng(1234)
@@ -330,8 +330,9 @@ def test_gated_special_gates():
 
 
 def test_weight_grad_column_subset_and_rows_order_free_of_layout():
-    """The weight gradient is per column: slicing columns commutes with it, and the
-    fp32 result is the rounding of the double sum (checked against rationals)."""
+    """The weight gradient is per column: slicing columns commutes with it, and
+    the result is an fp32 value ([Residual], Implementation: the weight gradient
+    is fp32), the one nearest the exact sum (checked against rationals)."""
     T, D = 5, 8
     x = _bf16_grid(RNG.standard_normal((T, D)))
     g = _bf16_grid(RNG.standard_normal((T, D)))
@@ -340,6 +341,7 @@ def test_weight_grad_column_subset_and_rows_order_free_of_layout():
     for j in range(D):
         exact = sum(Fraction(g[t, j]) * Fraction(x[t, j]) * Fraction(r[t]) for t in range(T))
         assert abs(Fraction(dw[j]) - exact) <= abs(exact) * Fraction(1, 2**23) + Fraction(1, 2**140)
+        assert dw[j] == fp32_round_exact(exact), j
 
 
 # ==========================================================================
@@ -384,6 +386,38 @@ def test_fused_add_rounding_bruteforce(zc):
     np.testing.assert_array_equal(y0, yp)
     np.testing.assert_array_equal(r0, rp)
     np.testing.assert_array_equal(ro0, x)
+
+
+def test_fused_add_sum_is_rounded_to_fp32_before_the_norm():
+    """The norm is taken over the fp32 sum h = fl32(x + res), not over the exact
+    sum (the reading of [ZC-norm]'s fused add: one fp32 add). Rows whose residual
+    dwarfs x (an exponent gap of about 20, so x + res needs more than 24 bits)
+    are drawn until some of them have a different correctly rounded rstd for the
+    fp32 sum than for the exact one; on every row the oracle's rstd must be the
+    one of the fp32 sum, and y follows from it."""
+    getcontext().prec = 60
+    T, D = 96, 8
+    rng = np.random.default_rng(77)
+    res = _bf16_grid(rng.standard_normal((T, D)) * 2.0**12)
+    x = _bf16_grid(rng.standard_normal((T, D)) * 2.0**-8)
+    w = np.float32(rng.standard_normal(D) * 0.3 + 1.0).astype(np.float64)
+    eps = Fraction(float(np.float32(1e-6)))
+    y, rstd, _ = oracle.fused_add_fwd(x, res, w, 1e-6)
+
+    def rstd_of(h):
+        ms = sum(Fraction(v) ** 2 for v in h) / D + eps
+        return fp32_round_exact(Fraction(Decimal(1) / (Decimal(ms.numerator) / Decimal(ms.denominator)).sqrt()))
+
+    telling = 0
+    for t in range(T):
+        exact = [Fraction(x[t, j]) + Fraction(res[t, j]) for j in range(D)]  # exact in double too
+        h32 = [float(np.float32(float(v))) for v in exact]
+        want = rstd_of(h32)
+        telling += want != rstd_of(exact)
+        assert rstd[t] == want, t
+        for j in range(D):
+            assert y[t, j] == bf16_round_bruteforce(Fraction(h32[j]) * Fraction(rstd[t]) * Fraction(w[j]))
+    assert telling >= 4, telling  # the case tells the two sums apart
 
 
 # ==========================================================================
