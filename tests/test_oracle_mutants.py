@@ -42,13 +42,23 @@ MUTANTS = [
     ("f16_one_bit_short", "int q = (e < -14) ? -24 : e - 10;", "int q = (e < -14) ? -24 : e - 11;"),
     ("f16_subnormal_quantum", "int q = (e < -14) ? -24 : e - 10;", "int q = (e < -14) ? -25 : e - 10;"),
     ("f16_overflow_late", "if (r >= ldexp(1.0, 16)) r = INFINITY;", "if (r > ldexp(1.0, 16)) r = INFINITY;"),
+    ("act_format_bf16_as_f16", "if (rounded == 1) return orc_round_bf16(v);", "if (rounded == 1) return orc_round_f16(v);"),
+    ("act_format_f16_as_bf16", "if (rounded == 2) return orc_round_f16(v);", "if (rounded == 2) return orc_round_bf16(v);"),
     # inverse RMS
     ("sum_of_abs", "ss += x[j] * x[j];", "ss += fabs(x[j]);"),
+    ("sum_skips_first", "for (int64_t j = 0; j < D; ++j) ss += x[j] * x[j];",
+     "for (int64_t j = 1; j < D; ++j) ss += x[j] * x[j];"),
     ("mean_over_d_minus_1", "double mean = ss / (double)D;", "double mean = ss / (double)(D - 1);"),
     ("eps_outside_root", "return 1.0 / sqrt(mean + eps);", "return 1.0 / (sqrt(mean) + eps);"),
     ("rstd_not_fp32",
      "double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);\n        rstd[t] = r;\n        for (int64_t j = 0; j < D; ++j)\n",
      "double r = row_inv_rms(xr, D, eps);\n        rstd[t] = r;\n        for (int64_t j = 0; j < D; ++j)\n"),
+    ("gated_rstd_not_fp32",
+     "double r = maybe_fl32(row_inv_rms(xr, D, eps), rounded);\n        rstd[t] = r;\n        for (int64_t j = 0; j < D; ++j) {\n",
+     "double r = row_inv_rms(xr, D, eps);\n        rstd[t] = r;\n        for (int64_t j = 0; j < D; ++j) {\n"),
+    ("fused_rstd_not_fp32", "double r = maybe_fl32(row_inv_rms(h, D, eps), rounded);", "double r = row_inv_rms(h, D, eps);"),
+    ("hf_rstd_not_fp32", "rstd[t] = maybe_fl32(row_inv_rms(x + t * D, D, eps), rounded);",
+     "rstd[t] = row_inv_rms(x + t * D, D, eps);"),
     # effective weight
     ("zc_offset_dropped", "return maybe_fl32(w + 1.0, rounded);", "return maybe_fl32(w, rounded);"),
     ("zc_offset_not_fp32", "return maybe_fl32(w + 1.0, rounded);", "return w + 1.0;"),
@@ -72,6 +82,8 @@ MUTANTS = [
     # weight gradient
     ("dw_drops_r", "double term = gt * x[t * D + j] * r[t];", "double term = gt * x[t * D + j];"),
     ("dw_not_fp32", "dw[j] = maybe_fl32(acc, rounded);", "dw[j] = acc;"),
+    ("dw_keeps_last_term", "acc += term;", "acc = term;"),
+    ("dw_transposed_x", "double term = gt * x[t * D + j] * r[t];", "double term = gt * x[j * T + t] * r[t];"),
     ("dw_ignores_gate", "if (z) gt *= gate_q(z[t * D + j], gate);", "if (z) gt *= 1.0;"),
     # gates
     ("sigmoid_sign", "static double sigmoid(double z) { return 1.0 / (1.0 + exp(-z)); }",
@@ -86,6 +98,8 @@ MUTANTS = [
     ("gated_dot_without_gate", "double term = gr[i] * gate_q(zr[i], gate) * xr[i] * w_eff(w[i], zero_centered, rounded);",
      "double term = gr[i] * xr[i] * w_eff(w[i], zero_centered, rounded);"),
     ("gated_dz_drops_r", "double u = xr[k] * r * we;", "double u = xr[k] * we;"),
+    ("gated_bwd_ignores_zc", "double we = w_eff(w[k], zero_centered, rounded);", "double we = w[k];"),
+    ("gated_fwd_ignores_zc", "double u = xr[j] * r * w_eff(w[j], zero_centered, rounded);", "double u = xr[j] * r * w[j];"),
     ("gated_fwd_drops_gate", "y[t * D + j] = maybe_act(u * gate_q(z[t * D + j], gate), rounded);",
      "y[t * D + j] = maybe_act(u, rounded);"),
     # fused add + norm
@@ -95,6 +109,7 @@ MUTANTS = [
      "for (int64_t j = 0; j < D; ++j) h[j] = maybe_fl32(x[t * D + j] + res[t * D + j], rounded);",
      "for (int64_t j = 0; j < D; ++j) h[j] = maybe_act(x[t * D + j] + res[t * D + j], rounded);"),
     ("fused_res_out_unrounded", "h[j] = maybe_act(h[j], rounded);", "h[j] = h[j];"),
+    ("fused_bwd_at_x", "orc_rmsnorm_bwd(T, D, g, h_scratch, w,", "orc_rmsnorm_bwd(T, D, g, x, w,"),
     ("fused_bwd_drops_res", "h_scratch[t * D + j] = maybe_fl32(x[t * D + j] + res[t * D + j], rounded);",
      "h_scratch[t * D + j] = maybe_fl32(x[t * D + j], rounded);"),
     # HF-convention gated forward
