@@ -9,7 +9,7 @@ the pin suites (``tests/test_oracle_pins.py``, ``tests/test_oracle_pins_options.
 run against it in a child process (the oracle package loads the library that
 ``RMSN_ORACLE_LIB`` names). The test requires every such run to fail. A
 mistake no pin notices would mean the oracle could carry it unseen into every
-parity verdict.
+parity comparison.
 
 Sources the mistakes refer to: [Megatron] Megatron-LM pull request 6859 "Fix
 the batch-invariant RMSNorm forward and its input gradient" (item 1: the
