@@ -5,11 +5,16 @@ Nothing here computes the normalisation; it only converts and compares.
 from __future__ import annotations
 
 import bisect
+import glob
 import math
+import os
+import re
 from fractions import Fraction
 
 import numpy as np
 import torch
+
+ROOT_DIR = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 
 def to_f64(t: torch.Tensor) -> np.ndarray:
@@ -392,3 +397,15 @@ def dx_model(g, h, w_eff, r, mode: str, g_res=None, fmt: str = "bf16"):
     if g_res is not None:
         d = d + g_res
     return f32_round_act(d, fmt)
+
+
+def header_declarations(root: str = ROOT_DIR):
+    """(return type, name, [parameter types]) of every entry point in include/*.h."""
+    out = []
+    for h in glob.glob(os.path.join(root, "include", "*.h")):
+        txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
+        txt = "\n".join(l for l in txt.split("\n") if not l.strip().startswith("#"))
+        for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\b(rmsnorm_\w+)\s*\(([^)]*)\)\s*;", txt):
+            types = [re.sub(r"\b\w+$", "", q.strip()).strip() for q in params.split(",") if q.strip()]
+            out.append((" ".join(ret.split()).replace(" *", "*"), name, types))
+    return out

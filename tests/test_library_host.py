@@ -15,6 +15,7 @@ import pytest
 
 import invariant_rmsnorm_gb300 as rn
 from invariant_rmsnorm_gb300 import build as cuda_build
+from tests._helpers import header_declarations
 
 ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
@@ -42,18 +43,6 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
 
 
-def _declarations():
-    """(return type, name, [parameter types]) of every entry point in include/*.h."""
-    out = []
-    for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
-        txt = re.sub(r"/\*.*?\*/", "", open(h).read(), flags=re.S)
-        txt = "\n".join(l for l in txt.split("\n") if not l.strip().startswith("#"))
-        for ret, name, params in re.findall(r"([A-Za-z_][\w\s\*]*?)\b(rmsnorm_\w+)\s*\(([^)]*)\)\s*;", txt):
-            types = [re.sub(r"\b\w+$", "", q.strip()).strip() for q in params.split(",") if q.strip()]
-            out.append((" ".join(ret.split()).replace(" *", "*"), name, types))
-    return out
-
-
 _SCALARS = {"int": ctypes.c_int, "int64_t": ctypes.c_int64, "float": ctypes.c_float, "size_t": ctypes.c_size_t,
             "unsigned long long": ctypes.c_ulonglong, "rmsn_stream": ctypes.c_void_p}
 
@@ -69,7 +58,7 @@ def test_binding_signatures_match_the_header(lib):
     and, position by position, a type of the same kind and width (a pointer, or
     the same integer / float type), and the same return type: a mismatch would
     pass garbage through the C ABI without any error."""
-    decls = _declarations()
+    decls = header_declarations()
     assert {n for _, n, _ in decls} == set(rn.EXPORTED_SYMBOLS)
     for ret, name, types in decls:
         res, args = rn._SIGS[name]
