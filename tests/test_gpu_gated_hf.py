@@ -3,7 +3,6 @@ divergence in the zero-centred RMSNorm PR, RL-Kernel pull request 467) against
 the float64 oracle, and the divergence itself measured on the GPU."""
 from __future__ import annotations
 
-import numpy as np
 import pytest
 import torch
 

@@ -14,7 +14,7 @@ import pytest
 import torch
 
 from invariant_rmsnorm_gb300 import synth
-from tests.gpu_common import DEV, check_bwd, check_fwd, run_bwd, run_fwd
+from tests.gpu_common import DEV, check_fwd, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
