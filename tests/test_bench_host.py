@@ -23,3 +23,16 @@ def test_both_arms_report_the_same_config():
     c = bench.residual_config(1)
     assert c["T"] == 32768 and c["D"] == 4096 and c["workload"] == "rmsnorm_residual fwd+bwd"
     assert bench.residual_config(4)["parallelism"] == "replicas x4"
+
+
+def test_algorithmic_bytes_count_each_tensor_once():
+    """The roofline numerators, rebuilt from the tensors each kernel must move
+    once: bf16 activations of 2 bytes, an fp32 rstd of 4 bytes per row (w and
+    dgamma, [D] each, are left out as negligible)."""
+    T, D = 32768, 4096
+    act, rstd = 2 * D, 4
+    fwd = (act) + (act + act + rstd)                   # x in; y, x_copy, rstd out
+    bwd = (act + act + act + rstd) + (act)             # g, x, g_res, rstd in; dx out
+    assert bench.fwd_bytes(T, D) == T * fwd
+    assert bench.bwd_pass1_bytes(T, D) == T * bwd
+    assert bench.step_bytes(T, D) == T * (fwd + bwd) == 1_879_310_336
