@@ -41,6 +41,9 @@ MUTANTS = [
     ("bf16_subnormal_quantum", "int q = (e < -126) ? -133 : e - 7;", "int q = (e < -126) ? -134 : e - 7;"),
     ("f16_one_bit_short", "int q = (e < -14) ? -24 : e - 10;", "int q = (e < -14) ? -24 : e - 11;"),
     ("f16_subnormal_quantum", "int q = (e < -14) ? -24 : e - 10;", "int q = (e < -14) ? -25 : e - 10;"),
+    ("f16_ties_away", "double r = ldexp(nearbyint(ldexp(a, -q)), q);", "double r = ldexp(floor(ldexp(a, -q) + 0.5), q);"),
+    ("f16_truncates", "double r = ldexp(nearbyint(ldexp(a, -q)), q);", "double r = ldexp(trunc(ldexp(a, -q)), q);"),
+    ("bf16_truncates", "double nr = nearbyint(n);", "double nr = trunc(n);"),
     ("f16_overflow_late", "if (r >= ldexp(1.0, 16)) r = INFINITY;", "if (r > ldexp(1.0, 16)) r = INFINITY;"),
     ("act_format_bf16_as_f16", "if (rounded == 1) return orc_round_bf16(v);", "if (rounded == 1) return orc_round_f16(v);"),
     ("act_format_f16_as_bf16", "if (rounded == 2) return orc_round_f16(v);", "if (rounded == 2) return orc_round_bf16(v);"),
