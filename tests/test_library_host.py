@@ -215,6 +215,25 @@ def test_selftest_wait_validation_rejects_before_launch(lib):
     assert rn.DEVICE_ERR_WAIT_TIMEOUT == 1
 
 
+def test_product_sources_never_reach_the_oracle():
+    """No file of the package (Python, CUDA, headers) imports, includes or
+    loads anything under oracle/, and the oracle includes nothing of the
+    library: the two share no code."""
+    import ast
+    pkg = os.path.join(ROOT, "invariant_rmsnorm_gb300")
+    for path in glob.glob(os.path.join(pkg, "*.py")):
+        for node in ast.walk(ast.parse(open(path).read())):
+            if isinstance(node, ast.Import):
+                assert not any(a.name.split(".")[0] == "oracle" for a in node.names), path
+            if isinstance(node, ast.ImportFrom):
+                assert (node.module or "").split(".")[0] != "oracle", path
+    for path in glob.glob(os.path.join(pkg, "csrc", "*")) + glob.glob(os.path.join(ROOT, "include", "*.h")):
+        for inc in re.findall(r'#\s*include\s*[<"]([^>"]+)[>"]', open(path).read()):
+            assert "oracle" not in inc, (path, inc)
+    for inc in re.findall(r'#\s*include\s*[<"]([^>"]+)[>"]', open(os.path.join(ROOT, "oracle", "rmsnorm_oracle.c")).read()):
+        assert inc in ("math.h", "stdint.h", "string.h", "omp.h"), inc
+
+
 def test_package_has_no_non_cuda_path():
     """The binding refuses to run without the built library (no fallback)."""
     import importlib
