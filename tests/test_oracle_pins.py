@@ -285,6 +285,33 @@ def test_residual_bwd_matches_finite_differences():
     assert np.array_equal(xcb, xb)
 
 
+@pytest.mark.parametrize("zc,residual", [(False, False), (True, False), (False, True)])
+def test_bwd_output_bits_bruteforce(zc, residual):
+    """In rounded mode dx is the bf16 value nearest the exact input gradient at
+    the saved fp32 rstd: g w_eff r - (r^3 x / D) sum_i g_i x_i w_eff_i [+ g_res]
+    ([Megatron], What does this PR do, item 2; [Residual], the reviewer's "for
+    dx"), evaluated with rationals and rounded once."""
+    T, D = 3, 16
+    x = _bf16_grid(RNG.standard_normal((T, D)))
+    g = _bf16_grid(RNG.standard_normal((T, D)))
+    gres = _bf16_grid(RNG.standard_normal((T, D))) if residual else None
+    w = np.float32(RNG.standard_normal(D) * 0.3 + (0.0 if zc else 1.0)).astype(np.float64)
+    _, r = oracle.rmsnorm_fwd(x, w, 1e-6, zero_centered_gamma=zc)
+    if residual:
+        dx, _ = oracle.residual_bwd(g, x, w, r, gres, zero_centered_gamma=zc)
+    else:
+        dx, _ = oracle.rmsnorm_bwd(g, x, w, r, zero_centered_gamma=zc)
+    weff = [Fraction(float(np.float32(v) + np.float32(1.0))) if zc else Fraction(v) for v in w]
+    for t in range(T):
+        rt = Fraction(r[t])
+        s = sum(Fraction(g[t, i]) * Fraction(x[t, i]) * weff[i] for i in range(D))
+        for k in range(D):
+            v = Fraction(g[t, k]) * weff[k] * rt - rt ** 3 * Fraction(x[t, k]) / D * s
+            if residual:
+                v += Fraction(gres[t, k])
+            assert dx[t, k] == bf16_round_bruteforce(v), (t, k)
+
+
 @pytest.mark.parametrize("zc", [False, True])
 def test_gated_bwd_matches_finite_differences(zc):
     """Gated norm: dx, dz and dweight against central differences of the forward."""
