@@ -473,6 +473,42 @@ def test_gated_hf_convention_divergence_matches_the_pages():
     np.testing.assert_array_equal(ye, yhe)
 
 
+def _bf16_rn(v):
+    """Nearest bf16 (ties to even) of normal doubles: 8 significant bits."""
+    m, e = np.frexp(v)
+    return np.ldexp(np.round(m * 256) / 256, e)
+
+
+def test_gated_hf_reading_is_a_choice_the_page_figure_does_not_make():
+    """The page gives no cast points for the HF-convention gated norm, only that
+    its weight multiply is not the vLLM one's fp32 multiply, and the 65 % figure.
+    Three readings, all with the normalised value cast to bf16, measured on the
+    page's setup (seed 0, randn weights): the oracle's (bf16 weight, product
+    rounded to bf16) agrees with the vLLM convention on 60.1 %; keeping the
+    product in fp32 with a bf16 weight gives 66.7 %; an fp32 weight and product
+    74.2 %. The page's band (65 % +- 15) takes all three, so it cannot choose
+    between them: these exact fractions make a change of the oracle's reading a
+    visible decision rather than a silent one."""
+    gold = _golden("zc_norm_gated_conventions.json")
+    g = torch.Generator().manual_seed(0)
+    x = torch.randn(gold["rows"], gold["D"], generator=g).to(torch.bfloat16).double().numpy()
+    z = torch.randn(gold["rows"], gold["D"], generator=g).to(torch.bfloat16).double().numpy()
+    w = np.float32(torch.randn(gold["D"], generator=g).double().numpy()).astype(np.float64)
+    yv, rv = oracle.gated_fwd(x, z, w, 1e-6, zero_centered_gamma=False)
+    yh, _ = oracle.gated_hf_fwd(x, z, w, 1e-6, zero_centered_gamma=False)
+    n = _bf16_rn(np.float32(x * rv[:, None]).astype(np.float64))   # the normalised value, cast to bf16
+    silu = z / (1.0 + np.exp(-z))
+    y_fp32_w = _bf16_rn(np.float32(w[None, :] * n).astype(np.float64) * silu)
+    y_bf16_w = _bf16_rn(np.float32(_bf16_rn(w)[None, :] * n).astype(np.float64) * silu)
+    fractions = {name: float(np.mean(y == yv)) for name, y in
+                 (("oracle", yh), ("bf16 weight, fp32 product", y_bf16_w), ("fp32 weight", y_fp32_w))}
+    assert abs(fractions["oracle"] - 0.601) < 0.005, fractions
+    assert abs(fractions["bf16 weight, fp32 product"] - 0.667) < 0.005, fractions
+    assert abs(fractions["fp32 weight"] - 0.742) < 0.005, fractions
+    for f in fractions.values():
+        assert abs(f - gold["same_fraction"]) < 0.15, fractions
+
+
 def test_gated_hf_rounding_points_bruteforce():
     """Each of the HF reading's casts, checked with rationals and the bf16 table."""
     T, D = 2, 16
