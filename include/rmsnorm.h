@@ -106,7 +106,7 @@ size_t rmsnorm_bwd_workspace_bytes(int64_t T, int64_t D);
 
 /* The largest rmsnorm_bwd_workspace_bytes(T, D) over 0 <= T <= T_max: one
  * buffer of this many bytes serves every such T (0 for T_max <= 0 or an
- * unsupported D). */
+ * unsupported D). Computed in closed form, in constant time for any T_max. */
 size_t rmsnorm_bwd_workspace_bytes_max(int64_t T_max, int64_t D);
 
 /* Backward, plain or zero-centred ([Megatron] item 2; [Residual] Backward).
@@ -140,7 +140,10 @@ int rmsnorm_residual_bwd(const rmsn_bf16* g, int64_t ldg, const rmsn_bf16* x, in
 
 /* Gated forward, Qwen3-Next / vLLM convention ([ZC-norm], gated-norm conventions):
  *   y = bf16( ((x * r) * w_eff) * silu(z) ), weight multiply and gate in fp32,
- *   silu(z) = z * (1 / (1 + expf(-z))).  z [T][ldz] in (the gate). */
+ *   silu(z) = z * sigmoid(z), sigmoid evaluated in fp32 in a two-sided form
+ *   from the PTX approximate instructions ex2 and rcp (relative error a few
+ *   fp32 ulp plus about |z| * 2^-24, far inside one bf16 ulp).
+ *   z [T][ldz] in (the gate). */
 int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz,
                       const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
                       int64_t T, int64_t D, float eps, int zero_centered_gamma,
@@ -319,11 +322,19 @@ int rmsnorm_dgamma_reduce(const void* ws, size_t ws_bytes, int64_t T, int64_t D,
  * every GPU that loads the library, held until the process exits. The call
  * allocates nothing; inputs and outputs are the caller's, as in rmsnorm_bwd
  * (same arguments minus the workspace; dgamma must not be NULL).
- *   - Problems needing more scratch than the array holds, i.e. with
- *     rmsnorm_bwd_workspace_bytes(T, D) > RMSN_NOALLOC_SCRATCH_BYTES, are
- *     rejected with RMSN_EWORKSPACE. Every T up to 32768 fits at D <= 4096.
+ *   - Arguments are checked as rmsnorm_bwd checks them, and fail with its
+ *     statuses; then a NULL dgamma is RMSN_EINVAL, and a problem needing more
+ *     scratch than the array holds, i.e. with
+ *     rmsnorm_bwd_workspace_bytes(T, D) > RMSN_NOALLOC_SCRATCH_BYTES, is
+ *     rejected with RMSN_EWORKSPACE. Every T up to T_max fits exactly when
+ *     rmsnorm_bwd_workspace_bytes_max(T_max, D) <= RMSN_NOALLOC_SCRATCH_BYTES:
+ *     every T <= 32768 at D <= 6896 and at 7176 <= D <= 8192 (D = 8192,
+ *     T = 32768 fills the array exactly), every T <= 29250 at
+ *     6904 <= D <= 7168 (shortened chunks), every T <= 16384 at D = 16384.
  *   - The first call on a device looks up the array's device address with
  *     that device current; make that first call before any stream capture.
+ *     A cudaDeviceReset destroys the context and can move the array; the
+ *     next call in the new context looks the address up again.
  *   - Every call shares the one array: calls whose work overlaps on the GPU
  *     (other streams or threads, unordered) race and corrupt dgamma. Calls on
  *     one stream are safe. Leftover contents are never read.

@@ -1,6 +1,7 @@
 // C-ABI layer: argument validation, row-shape selection, device caches and
 // dispatch to the kernel launchers. Every check runs on the host before any
 // launch; there is no fallback path.
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -84,6 +85,36 @@ int64_t wide_chunk_rows(int64_t T, int D) {
     const int64_t rounds = (n0 + ctas - 1) / ctas;
     if (10 * n0 >= 9 * rounds * ctas) return c0;
     return (T + rounds * ctas - 1) / (rounds * ctas);  // < 32
+}
+
+// The largest number of wide-path chunks over every row count 1..T_max, in
+// closed form (a loop over at most nine rounds). Chunks are shortened only in
+// rounds R = 2..9 of the nominal grid (from ten rounds on, 32-row chunks fill
+// over 90 % of their rounds), and there a row count t gets
+// c = ceil(t / (R K)) rows a chunk (K = 2 kBalanceSms) and ceil(t / c) <= R K
+// chunks, with exactly R K whenever t is a multiple of R K. So over the
+// shortened row counts of round R up to T_max (t_lo..t_top), the largest
+// count is R K if a multiple of R K lies in that range, and otherwise
+// ceil(t_top / c), since c is then the same for all of them and ceil(t / c)
+// grows with t. Every other row count has 32-row chunks, at most as many as
+// T_max has with 32-row chunks.
+int64_t wide_chunks_max(int64_t T_max, int D) {
+    constexpr int64_t c0 = kWideChunkRows;
+    if (T_max <= 0) return 0;
+    int64_t best = (T_max + wide_chunk_rows(T_max, D) - 1) / wide_chunk_rows(T_max, D);
+    best = std::max(best, (T_max + c0 - 1) / c0);
+    if (D <= 2048 || D > 7168) return best;
+    const int64_t K = kBalanceSms * 2;
+    for (int64_t R = 2; R <= 9; ++R) {
+        const int64_t t_lo = c0 * (R - 1) * K + 1;     // first row count of round R
+        const int64_t n_hi = (9 * R * K - 1) / 10;     // most 32-row chunks still under 90 % of R K
+        const int64_t t_top = std::min(T_max, c0 * n_hi);
+        if (t_top < t_lo) break;
+        const int64_t c_top = (t_top + R * K - 1) / (R * K);
+        if ((c_top - 1) * R * K >= t_lo) best = std::max(best, R * K);  // a multiple of R K in range
+        else best = std::max(best, (t_top + c_top - 1) / c_top);
+    }
+    return best;
 }
 
 int64_t num_chunks(int64_t T, int D) {
@@ -232,9 +263,12 @@ int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     // one-CTA-per-SM backward gets).
     if (!c.narrow && a.D / 8 >= RMSN_BWD_NT512_FROM && a.D / 8 <= 4 * RMSN_BWD_NTMAX)
         wide_shape(a.D / 8, 512, &c.bwd_threads, &c.bwd_vpt);
+    // The recompute of y is a compile-time flag of the kernels: the backward
+    // without it carries no y code (nor its registers).
+    const int mr = a.y != nullptr ? (m | kFlagRecompute) : m;
     cudaError_t e;
-    if (is_f16(m)) e = c.narrow ? launch_narrow_bwd_f16(m, a, c, s) : launch_wide_bwd_f16(m, a, c, s);
-    else e = c.narrow ? launch_narrow_bwd(m, a, c, s) : launch_wide_bwd(m, a, c, s);
+    if (is_f16(m)) e = c.narrow ? launch_narrow_bwd_f16(mr, a, c, s) : launch_wide_bwd_f16(mr, a, c, s);
+    else e = c.narrow ? launch_narrow_bwd(mr, a, c, s) : launch_wide_bwd(mr, a, c, s);
     if (e != cudaSuccess) return RMSN_ECUDA;
     const int64_t nchunks = c.narrow ? num_chunks(a.T, a.D) : (a.T + a.chunk - 1) / a.chunk;
     if (dgamma != nullptr) e = launch_dgamma_reduce(a.partials, nchunks, a.D, dgamma, s);
@@ -242,6 +276,21 @@ int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
 }
 
 }  // namespace
+
+// The backward's checks that come after the shape's and before the
+// workspace's, in rmsnorm_bwd's order (T >= 1 and D already checked).
+int rmsn::bwd_check_args(const uint16_t* g, int64_t ldg, const uint16_t* x, int64_t ldx, const float* w,
+                         const float* rstd, const uint16_t* dx, int64_t lddx, const float* dgamma, int64_t T,
+                         int64_t D) {
+    (void)T;
+    RMSN_TRY(check_act(g, ldg, D));
+    RMSN_TRY(check_act(x, ldx, D));
+    RMSN_TRY(check_act(dx, lddx, D));
+    RMSN_TRY(check_vec(w));
+    RMSN_TRY(check_vec(rstd));
+    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    return RMSN_OK;
+}
 
 // ---------------------------------------------------------------------------
 // The operations, with the variant flags (activation dtype, gate) as the first
@@ -303,12 +352,7 @@ int rmsnorm_bwd_impl(int flags, const rmsn_act16* g, int64_t ldg, const rmsn_act
                      int64_t T, int64_t D, int zero_centered_gamma, rmsn_stream stream) {
     RMSN_TRY(check_shape(T, D));
     if (T == 0) return RMSN_OK;
-    RMSN_TRY(check_act(g, ldg, D));
-    RMSN_TRY(check_act(x, ldx, D));
-    RMSN_TRY(check_act(dx, lddx, D));
-    RMSN_TRY(check_vec(w));
-    RMSN_TRY(check_vec(rstd));
-    if (dgamma) RMSN_TRY(check_vec(dgamma));
+    RMSN_TRY(bwd_check_args(g, ldg, x, ldx, w, rstd, dx, lddx, dgamma, T, D));
     RMSN_TRY(check_ws(ws, ws_bytes, T, D));
     BwdArgs a{};
     a.g = g; a.ldg = ldg; a.x = x; a.ldx = ldx; a.w = w; a.rstd = rstd; a.dx = dx; a.lddx = lddx;

@@ -140,19 +140,30 @@ __device__ __forceinline__ int named_bar_and(int id, int nthreads, int pred) {
 // Bounded wait for the phase with parity `parity` to complete. Returns false if
 // `limit_ns` (the kernels use kWaitTimeoutNs) of global time elapsed without
 // completion.
+#ifndef RMSN_WAIT_HINT_NS
+#define RMSN_WAIT_HINT_NS 0  // suspend-time hint of each try_wait (0: the hardware's default)
+#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           unsigned long long limit_ns = kWaitTimeoutNs) {
     const uint32_t addr = smem_u32(bar);
     uint32_t done = 0;
     unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
+#if RMSN_WAIT_HINT_NS
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(addr), "r"(parity), "n"(RMSN_WAIT_HINT_NS) : "memory");
+#else
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
             "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done) : "r"(addr), "r"(parity) : "memory");
+#endif
         if (done) return true;
-        if ((it & 255u) == 0u) {
+        if (RMSN_WAIT_HINT_NS || (it & 255u) == 0u) {  // with a hint, every try sleeps: check each time
             const unsigned long long now = global_timer_ns();
             if (it == 0) t0 = now;
             else if (now - t0 > limit_ns) return false;
@@ -344,21 +355,21 @@ __device__ __forceinline__ float2 pair(const float* v, int e) { return make_floa
 __device__ __forceinline__ float2 both(float v) { return make_float2(v, v); }
 
 // e^-a for a >= 0, from the PTX instruction ex2.approx.ftz.f32 (2^x, which
-// flushes subnormal results to zero): e^-a = 2^t with t = -a log2(e). For
-// t < -64 the argument is raised by 64 and the result scaled back by an exact
-// multiply with 2^-64, so results down to the smallest fp32 subnormal (reached
-// at a of about 103) are kept rather than flushed. Relative error about
-// (2 + 2a) * 2^-24: 2 ulp from the instruction, the rest from rounding t.
+// flushes subnormal results to zero), as the square of a half-way power:
+// h = 2^(-a log2(e) / 2), e^-a = h * h. h stays a normal number for every a
+// up to about 174, so the flush never bites where e^-a is still an fp32
+// value (down to the smallest subnormal, reached at a of about 103): the
+// square, an ordinary multiply that keeps subnormals, rounds those tails.
+// Relative error about (5 + a) * 2^-24: twice the instruction's error plus the
+// rounding of the exponent, doubled by the square, plus the square's rounding.
 #ifndef RMSN_FAST_EXP
 #define RMSN_FAST_EXP 1
 #endif
 __device__ __forceinline__ float exp_neg(float a) {
 #if RMSN_FAST_EXP
-    const float t = fmul(a, -1.4426950408889634f);
-    const bool low = t < -64.0f;
-    float r;
-    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(low ? fadd(t, 64.0f) : t));
-    return low ? fmul(r, 5.42101086242752217e-20f) : r;
+    float h;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(h) : "f"(fmul(a, -0.72134752044448170f)));
+    return fmul(h, h);
 #else
     return __expf(-a);
 #endif
@@ -379,18 +390,20 @@ __device__ __forceinline__ float rcp_1to2(float d) {
 // sigmoid(z) = 1 / (1 + exp(-z)) in fp32, in the stable two-sided form: with
 // e = exp(-|z|) in (0, 1] and s = 1 / (1 + e), sigmoid is s for z >= 0 and
 // e * s (= e^z / (1 + e^z)) for z < 0, so the divisor stays in [1, 2]. A
-// relative error of about (5 + 2|z|) * 2^-24 on sigmoid, for every finite z.
+// relative error of about (8 + |z|) * 2^-24 on sigmoid, for every finite z.
 __device__ __forceinline__ float sigmoidf_rn(float z) {
     const float e = exp_neg(fabsf(z));
     const float s = rcp_1to2(fadd(1.0f, e));
     return z >= 0.0f ? s : fmul(e, s);
 }
 
-// The gate q(z) of the gated norm and its derivative, from one exponential:
-//   silu:    q = z sigmoid(z),  q' = sigmoid(z) (1 + z (1 - sigmoid(z)))
-//   sigmoid: q = sigmoid(z),    q' = sigmoid(z) sigmoid(-z) = e s^2
-// (with e, s as in sigmoidf_rn; the product form has no cancellation in
-// either tail, where 1 - sigmoid(z) would lose every bit for z >> 0).
+// The gate q(z) of the gated norm and its derivative, from one exponential.
+// With e, s as in sigmoidf_rn, both sigmoid(z) and sigmoid(-z) = 1 - sigmoid(z)
+// come without a subtraction: one is s, the other e * s.
+//   silu:    q = z sigmoid(z),  q' = sigmoid(z) + q sigmoid(-z)
+//   sigmoid: q = sigmoid(z),    q' = sigmoid(z) sigmoid(-z) = (e s) s
+// (q is bit for bit gate_value's; neither form cancels in a tail, where
+// 1 - sigmoid(z) would lose every bit for z >> 0).
 template <bool SIG>
 __device__ __forceinline__ float gate_value(float z) {
     return SIG ? sigmoidf_rn(z) : fmul(z, sigmoidf_rn(z));
@@ -399,13 +412,15 @@ template <bool SIG>
 __device__ __forceinline__ void gate_eval(float z, float& q, float& dq) {
     const float e = exp_neg(fabsf(z));
     const float s = rcp_1to2(fadd(1.0f, e));
-    const float sg = z >= 0.0f ? s : fmul(e, s);
+    const float es = fmul(e, s);
+    const bool pos = z >= 0.0f;
+    const float sg = pos ? s : es;  // sigmoid(z)
     if (SIG) {
         q = sg;
-        dq = fmul(e, fmul(s, s));
+        dq = fmul(es, s);
     } else {
         q = fmul(z, sg);
-        dq = fmul(sg, fadd(1.0f, fmul(z, fsub(1.0f, sg))));
+        dq = fadd(sg, fmul(q, pos ? es : s));
     }
 }
 

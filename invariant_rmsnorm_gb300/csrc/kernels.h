@@ -20,10 +20,14 @@ enum Mode : int { kPlain = 0, kResidual = 1, kGated = 2, kFusedAdd = 3, kFusedAd
 constexpr int kModeMask = 0xff;
 constexpr int kFlagF16 = 0x100;
 constexpr int kFlagSigmoid = 0x200;
+// The backward that also writes the forward output y again (recompute), as a
+// compile-time flag, so that the other backward kernels carry no y code.
+constexpr int kFlagRecompute = 0x400;
 
 __host__ __device__ constexpr int base_mode(int mode) { return mode & kModeMask; }
 __host__ __device__ constexpr bool is_f16(int mode) { return (mode & kFlagF16) != 0; }
 __host__ __device__ constexpr bool is_sigmoid_gate(int mode) { return (mode & kFlagSigmoid) != 0; }
+__host__ __device__ constexpr bool is_recompute(int mode) { return (mode & kFlagRecompute) != 0; }
 __host__ __device__ constexpr bool is_fused(int mode) {
     return base_mode(mode) == kFusedAdd || base_mode(mode) == kFusedAddNoGres;
 }
@@ -92,6 +96,8 @@ int64_t num_chunks(int64_t T, int D);
 // Rows per weight-gradient chunk of the wide backward (D > 256) for T rows:
 // a function of T and D only (see api.cu).
 int64_t wide_chunk_rows(int64_t T, int D);
+// The most chunks any row count 1..T_max gets on the wide path (closed form).
+int64_t wide_chunks_max(int64_t T_max, int D);
 // The rmsnorm_residual backward with the weight-gradient chunk of `chunk_T`
 // rows' problem instead of its own T (so that a slice of rows writes the same
 // chunk partials as the whole problem would); otherwise rmsnorm_residual_bwd_ex.
@@ -99,6 +105,11 @@ int residual_bwd_chunk_of(int64_t chunk_T, const uint16_t* g, int64_t ldg, const
                           const float* w, const float* rstd, const uint16_t* g_res, int64_t ldgr, uint16_t* dx,
                           int64_t lddx, void* ws, size_t ws_bytes, int64_t T, int64_t D, int zero_centered_gamma,
                           int dtype, cudaStream_t stream);
+
+// rmsnorm_bwd's argument checks after the shape's and before the workspace's
+// (pointers, row strides, alignment), in its order; RMSN_OK if all pass.
+int bwd_check_args(const uint16_t* g, int64_t ldg, const uint16_t* x, int64_t ldx, const float* w,
+                   const float* rstd, const uint16_t* dx, int64_t lddx, const float* dgamma, int64_t T, int64_t D);
 
 // Launchers (return the launch's cudaError_t; arguments already validated).
 // `m` is a Mode with its variant flags. The bf16 variants are instantiated in

@@ -100,6 +100,10 @@ cudaError_t launch_narrow_bwd(int md, const BwdArgs& a, const RowCfg& c, cudaStr
         case kResidual: return nbwd_dispatch<kResidual>(a, c, st);
         case kGated: return nbwd_dispatch<kGated>(a, c, st);
         case kGated | kFlagSigmoid: return nbwd_dispatch<kGated | kFlagSigmoid>(a, c, st);
+        case kPlain | kFlagRecompute: return nbwd_dispatch<kPlain | kFlagRecompute>(a, c, st);
+        case kResidual | kFlagRecompute: return nbwd_dispatch<kResidual | kFlagRecompute>(a, c, st);
+        case kGated | kFlagRecompute: return nbwd_dispatch<kGated | kFlagRecompute>(a, c, st);
+        case kGated | kFlagSigmoid | kFlagRecompute: return nbwd_dispatch<kGated | kFlagSigmoid | kFlagRecompute>(a, c, st);
         case kFusedAdd: return nbwd_dispatch<kFusedAdd>(a, c, st);
         case kFusedAddNoGres: return nbwd_dispatch<kFusedAddNoGres>(a, c, st);
         default: break;

@@ -28,6 +28,10 @@ cudaError_t launch_narrow_bwd_f16(int md, const BwdArgs& a, const RowCfg& c, cud
         case kResidual | H: return nbwd_dispatch<kResidual | H>(a, c, st);
         case kGated | H: return nbwd_dispatch<kGated | H>(a, c, st);
         case kGated | kFlagSigmoid | H: return nbwd_dispatch<kGated | kFlagSigmoid | H>(a, c, st);
+        case kPlain | kFlagRecompute | H: return nbwd_dispatch<kPlain | kFlagRecompute | H>(a, c, st);
+        case kResidual | kFlagRecompute | H: return nbwd_dispatch<kResidual | kFlagRecompute | H>(a, c, st);
+        case kGated | kFlagRecompute | H: return nbwd_dispatch<kGated | kFlagRecompute | H>(a, c, st);
+        case kGated | kFlagSigmoid | kFlagRecompute | H: return nbwd_dispatch<kGated | kFlagSigmoid | kFlagRecompute | H>(a, c, st);
         case kFusedAdd | H: return nbwd_dispatch<kFusedAdd | H>(a, c, st);
         case kFusedAddNoGres | H: return nbwd_dispatch<kFusedAddNoGres | H>(a, c, st);
         default: break;

@@ -50,6 +50,15 @@
 #ifndef RMSN_NARROW_BWD_MINB
 #define RMSN_NARROW_BWD_MINB 3  // backward CTAs that must fit on one SM (register budget)
 #endif
+#ifndef RMSN_NARROW_GATED_X2
+#define RMSN_NARROW_GATED_X2 0
+#endif
+#ifndef RMSN_NARROW_COMB_BUFS
+#define RMSN_NARROW_COMB_BUFS 2  // chunk-combine buffers of the backward (1: one more barrier per chunk)
+#endif
+#ifndef RMSN_NARROW_FWD_X2
+#define RMSN_NARROW_FWD_X2 0
+#endif
 
 namespace rmsn {
 
@@ -105,6 +114,15 @@ template <int G> __host__ __device__ constexpr int narrow_stage_rows() {
     return G == 32 ? 32
                    : (narrow_pass_rows<G>() > RMSN_NARROW_STAGE_ROWS ? narrow_pass_rows<G>() : RMSN_NARROW_STAGE_ROWS);
 }
+// The forward streams at most two operands, so its stages can be longer: each
+// lane then handles more rows per stage wait and release (262144 x 128 gated:
+// 33.2 -> 31.5 us with 64-row stages).
+#ifndef RMSN_NARROW_FWD_STAGE_ROWS
+#define RMSN_NARROW_FWD_STAGE_ROWS 64
+#endif
+template <int G> __host__ __device__ constexpr int narrow_fwd_stage_rows() {
+    return narrow_pass_rows<G>() > RMSN_NARROW_FWD_STAGE_ROWS ? narrow_pass_rows<G>() : RMSN_NARROW_FWD_STAGE_ROWS;
+}
 template <int G> __host__ __device__ constexpr int narrow_chunk_rows() {
     return narrow_stage_rows<G>() > kNarrowChunkRowsMin ? narrow_stage_rows<G>() : kNarrowChunkRowsMin;
 }
@@ -159,8 +177,9 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
     static_assert(!(M == kGatedHF && F16), "the HF-convention witness is a bf16 forward");
     constexpr int NIN = fwd_inputs(MODE);
     constexpr int P = narrow_pass_rows<G>();
-    constexpr int RS = narrow_stage_rows<G>();
+    constexpr int RS = narrow_fwd_stage_rows<G>();
     constexpr int NP = RS / P;
+    constexpr bool FX2 = RMSN_F32X2 && RMSN_NARROW_FWD_X2;  // gated output products in packed pairs
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -231,6 +250,15 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
             }
             float f[8];
             narrow_norm_input<MODE>(xv, zv, f);  // x, or h = x + res
+            // The gate does not depend on the row's statistic: evaluated here, it
+            // overlaps the row reduction instead of following it.
+            float q[8];
+            if (is_gated(MODE)) {
+                float zf[8];
+                unpack_act<F16>(zv, zf);
+#pragma unroll
+                for (int e = 0; e < 8; ++e) q[e] = M == kGatedHF ? fmul(zf[e], sigmoidf_rn(zf[e])) : gate_value<SIG>(zf[e]);
+            }
             float ss = 0.0f;
 #pragma unroll
             for (int e = 0; e < 8; ++e) ss = fadd(ss, fmul(f[e], f[e]));
@@ -242,22 +270,24 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 if (lane_valid) {
                     float o[8];
                     if (M == kGated) {
-                        float zf[8];
-                        unpack_act<F16>(zv, zf);
+                        if constexpr (FX2) {
 #pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            const float q = gate_value<SIG>(zf[e]);
-                            o[e] = fmul(fmul(fmul(f[e], r), we[e]), q);
+                            for (int e = 0; e < 8; e += 2) {
+                                const float2 o2 = fmul2(fmul2(fmul2(pair(f, e), both(r)), pair(we, e)), pair(q, e));
+                                o[e] = o2.x;
+                                o[e + 1] = o2.y;
+                            }
+                        } else {
+#pragma unroll
+                            for (int e = 0; e < 8; ++e) o[e] = fmul(fmul(fmul(f[e], r), we[e]), q[e]);
                         }
                     } else if (M == kGatedHF) {
                         // HF convention: normalised value and weight multiply in bf16.
-                        float zf[8];
-                        unpack8(zv, zf);
 #pragma unroll
                         for (int e = 0; e < 8; ++e) {
                             const float n = round_bf16f(fmul(f[e], r));
                             const float t = round_bf16f(fmul(round_bf16f(we[e]), n));
-                            o[e] = fmul(t, fmul(zf[e], sigmoidf_rn(zf[e])));
+                            o[e] = fmul(t, q[e]);
                         }
                     } else {
 #pragma unroll
@@ -292,6 +322,8 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
     constexpr int NP = RS / P;
     constexpr int CN = narrow_chunk_rows<G>();
     constexpr int NSC = CN / RS;  // stages per chunk
+    constexpr bool RY = is_recompute(MODE);  // also write y (a.y is then not null)
+    constexpr bool NX2 = RMSN_F32X2 && RMSN_NARROW_GATED_X2 && M == kGated;
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -382,56 +414,110 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&empty[s]);
             }
-            float gf[8], xf[8], tf[8], q[8], dq[8], g0[8], ff[8];
+            // gf: g, or g q(z) (gated); gd (gated): g q'(z). The gate is evaluated
+            // once, before the row reduction; after it only gf, gd, x and the
+            // packed z (for the optional y) are needed.
+            float gf[8], xf[8], tf[8], ff[8], gd[8];
             unpack_act<F16>(gv, gf);
             narrow_norm_input<MODE>(xv, tv, xf);  // x, or h = x + res
-            if (M == kResidual || M == kGated) unpack_act<F16>(tv, tf);
+            if (M == kResidual) unpack_act<F16>(tv, tf);
             if (M == kFusedAdd) unpack_act<F16>(fv, ff);
             if (M == kGated) {
+                float zf[8], q[8], dq[8];
+                unpack_act<F16>(tv, zf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    g0[e] = gf[e];
-                    gate_eval<SIG>(tf[e], q[e], dq[e]);
-                    gf[e] = fmul(gf[e], q[e]);  // g * q(z)
+                for (int e = 0; e < 8; ++e) gate_eval<SIG>(zf[e], q[e], dq[e]);
+#pragma unroll
+                for (int e = 0; e < 8; e += 2) {
+                    if constexpr (NX2) {
+                        const float2 d2 = fmul2(pair(gf, e), pair(dq, e)), g2 = fmul2(pair(gf, e), pair(q, e));
+                        gd[e] = d2.x; gd[e + 1] = d2.y;  // g q'(z)
+                        gf[e] = g2.x; gf[e + 1] = g2.y;  // g q(z)
+                    } else {
+                        gd[e] = fmul(gf[e], dq[e]);
+                        gd[e + 1] = fmul(gf[e + 1], dq[e + 1]);
+                        gf[e] = fmul(gf[e], q[e]);
+                        gf[e + 1] = fmul(gf[e + 1], q[e + 1]);
+                    }
                 }
             }
             float gw[8];
             float sp = 0.0f;
+            if constexpr (NX2) {
 #pragma unroll
-            for (int e = 0; e < 8; ++e) {
-                gw[e] = fmul(gf[e], we[e]);
-                sp = fadd(sp, fmul(gw[e], xf[e]));
+                for (int e = 0; e < 8; e += 2) {  // products packed, s in ascending element order
+                    const float2 gw2 = fmul2(pair(gf, e), pair(we, e));
+                    gw[e] = gw2.x; gw[e + 1] = gw2.y;
+                    const float2 t2 = fmul2(gw2, pair(xf, e));
+                    sp = fadd(fadd(sp, t2.x), t2.y);
+                }
+            } else {
+#pragma unroll
+                for (int e = 0; e < 8; ++e) {
+                    gw[e] = fmul(gf[e], we[e]);
+                    sp = fadd(sp, fmul(gw[e], xf[e]));
+                }
             }
             sp = group_sum<G>(sp);
             const float coef = fmul(div_by_d(fmul(fmul(r, r), r), D, a.inv_d_pow2), sp);
             const int64_t row = row0 + rs_;
             if (row < T && lane_valid) {
                 float o[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    float d = fsub(fmul(gw[e], r), fmul(xf[e], coef));
-                    if (M == kResidual) d = fadd(d, tf[e]);
-                    if (M == kFusedAdd) d = fadd(d, ff[e]);
-                    o[e] = d;
-                    acc[e] = fadd(acc[e], fmul(fmul(gf[e], xf[e]), r));
-                }
-                st_global_cs(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
                 if (M == kGated) {
-                    float dzv[8], yv[8];
+                    // dx; dw term (g q) (x r); dz = (g q') u with u = (x r) w_eff; y = u q.
+                    float dzv[8];
+                    if constexpr (NX2) {
+                        const float2 r2 = both(r), c2 = both(coef);
+#pragma unroll
+                        for (int e = 0; e < 8; e += 2) {  // products packed, their sums scalar
+                            const float2 p2 = fmul2(pair(gw, e), r2), q2 = fmul2(pair(xf, e), c2);
+                            o[e] = fsub(p2.x, q2.x);
+                            o[e + 1] = fsub(p2.y, q2.y);
+                            const float2 xr = fmul2(pair(xf, e), r2);
+                            const float2 t2 = fmul2(pair(gf, e), xr);
+                            acc[e] = fadd(acc[e], t2.x);
+                            acc[e + 1] = fadd(acc[e + 1], t2.y);
+                            const float2 dz2 = fmul2(pair(gd, e), fmul2(xr, pair(we, e)));
+                            dzv[e] = dz2.x;
+                            dzv[e + 1] = dz2.y;
+                        }
+                    } else {
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            o[e] = fsub(fmul(gw[e], r), fmul(xf[e], coef));
+                            const float xr = fmul(xf[e], r);
+                            acc[e] = fadd(acc[e], fmul(gf[e], xr));
+                            dzv[e] = fmul(gd[e], fmul(xr, we[e]));
+                        }
+                    }
+                    st_global_cs(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
+                    st_global_cs(a.dz + row * a.lddz + 8 * l, pack_act<F16>(dzv));
+                    if constexpr (RY) {
+                        // The forward output again (the forward's operations, same bits).
+                        float zf[8], yv[8];
+                        unpack_act<F16>(tv, zf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e)
+                            yv[e] = fmul(fmul(fmul(xf[e], r), we[e]), gate_value<SIG>(zf[e]));
+                        st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
+                    }
+                } else {
 #pragma unroll
                     for (int e = 0; e < 8; ++e) {
-                        const float u = fmul(fmul(xf[e], r), we[e]);
-                        dzv[e] = fmul(fmul(g0[e], u), dq[e]);
-                        yv[e] = fmul(u, q[e]);
+                        float d = fsub(fmul(gw[e], r), fmul(xf[e], coef));
+                        if (M == kResidual) d = fadd(d, tf[e]);
+                        if (M == kFusedAdd) d = fadd(d, ff[e]);
+                        o[e] = d;
+                        acc[e] = fadd(acc[e], fmul(fmul(gf[e], xf[e]), r));
                     }
-                    st_global_cs(a.dz + row * a.lddz + 8 * l, pack_act<F16>(dzv));
-                    if (a.y) st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
-                } else if (a.y) {
-                    // The forward output again, from the saved rstd (same bits as the forward).
-                    float yv[8];
+                    st_global_cs(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
+                    if constexpr (RY) {
+                        // The forward output again, from the saved rstd (same bits as the forward).
+                        float yv[8];
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xf[e], r), we[e]);
-                    st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
+                        for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xf[e], r), we[e]);
+                        st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
+                    }
                 }
             }
         }
@@ -459,7 +545,15 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 for (int q = 1; q < P; ++q) t = fadd(t, cb[q * D + col]);
                 st_global_f1_hint(a.partials + chunk * D + col, t, keep);
             }
-            cbuf ^= 1;
+            if (RMSN_NARROW_COMB_BUFS == 1) {
+                // one buffer: everyone has read it before anyone writes the next chunk's totals
+                if (!named_bar_and(kNarrowConsumerBarrier, kNarrowThreads, 1)) {
+                    if (tid == 0) atomicOr(&g_narrow_error, kErrWaitTimeout);
+                    return;
+                }
+            } else {
+                cbuf ^= 1;
+            }
         }
     }
     pdl_release();
@@ -480,7 +574,7 @@ int narrow_stages(size_t budget, size_t stage, size_t fixed) {
 
 template <int MODE, int G>
 cudaError_t nfwd_t(const FwdArgs& a, cudaStream_t st) {
-    constexpr int RS = narrow_stage_rows<G>();
+    constexpr int RS = narrow_fwd_stage_rows<G>();
     constexpr int NIN = fwd_inputs(MODE);
     NarrowMaps m;
     std::memset(&m, 0, sizeof(m));
@@ -523,7 +617,7 @@ cudaError_t nbwd_t(const BwdArgs& a, cudaStream_t st) {
     if (e == cudaSuccess) e = encode_vec_1d(&m.rstd, a.rstd, a.T, RS);
     if (e != cudaSuccess) return e;
     const size_t stage = static_cast<size_t>(NIN) * RS * a.D * 2 + RS * 4;
-    const size_t fixed = static_cast<size_t>(2) * P * a.D * 4;
+    const size_t fixed = static_cast<size_t>(RMSN_NARROW_COMB_BUFS) * P * a.D * 4;
     const int S = narrow_stages(RMSN_NARROW_BWD_SMEM, stage, fixed);
     const size_t smem = S * (stage + 16) + fixed;
     if (smem > static_cast<size_t>(kMaxSmem)) return cudaErrorInvalidConfiguration;

@@ -11,12 +11,17 @@
 // The array is RMSN_NOALLOC_SCRATCH_BYTES (32 MiB) on every GPU where the
 // library's device code is loaded, held until the process exits. Its device
 // address is looked up once per device, on the first call made with that
-// device current (so that first call should come before any stream capture).
+// device current (so that first call should come before any stream capture),
+// and again after the device's context has been destroyed and recreated
+// (cudaDeviceReset), which reloads the module and can move the array: the
+// address is kept with the context's unique id and used only in that context.
 // All calls share the array: two calls that overlap on the GPU (different
 // streams, or different host threads, without ordering between them) race on
 // it and give wrong weight gradients. Nothing in the array has to start at
 // zero: every partial row the backward reads was written earlier in the same
 // call, so the contents a previous call left behind are never used.
+#include <cudaTypedefs.h>
+
 #include <mutex>
 
 #include "common.cuh"
@@ -29,21 +34,54 @@ static __device__ __align__(256) unsigned char g_noalloc_scratch[RMSN_NOALLOC_SC
 
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mu;
-void* g_noalloc_ptr[kMaxDevices] = {};
+struct ScratchEntry {
+    unsigned long long ctx_id;  // unique id of the context the address belongs to (0: none yet)
+    void* ptr;
+};
+ScratchEntry g_noalloc[kMaxDevices] = {};
 
-// Device address of the scratch array on the current device. In host code the
-// array's name is only a host-side stand-in; the real address must come from
-// cudaGetSymbolAddress, made with the device current.
+// The current context's unique id, through the driver entry points (the
+// library does not link libcuda). False if the driver does not provide them.
+bool current_context_id(unsigned long long* id) {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
+
+// Device address of the scratch array in the current device's context. In
+// host code the array's name is only a host-side stand-in; the real address
+// must come from cudaGetSymbolAddress, made with the device current.
 int scratch_address(void** out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return RMSN_ECUDA;
+    // Before the runtime has made the device's context current there is no id:
+    // the lookup below then runs, and the id is kept from a later call.
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
     std::lock_guard<std::mutex> lk(g_noalloc_mu);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    ScratchEntry& e = g_noalloc[dev];
+    if (!have_ctx || e.ptr == nullptr || e.ctx_id != ctx) {
         void* p = nullptr;
         if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return RMSN_ECUDA;
-        g_noalloc_ptr[dev] = p;
+        e.ptr = p;
+        e.ctx_id = have_ctx ? ctx : 0;  // without a context id, look it up on every call
     }
-    *out = g_noalloc_ptr[dev];
+    *out = e.ptr;
     return RMSN_OK;
 }
 
@@ -54,6 +92,8 @@ extern "C" int rmsnorm_bwd_noalloc(const rmsn_bf16* g, int64_t ldg, const rmsn_b
                                    const float* w, const float* rstd, rmsn_bf16* dx, int64_t lddx,
                                    float* dgamma, int64_t T, int64_t D, int zero_centered_gamma,
                                    rmsn_stream stream) {
+    // rmsnorm_bwd's own checks first, in its order, so that a call fails with
+    // the status rmsnorm_bwd would give; then this entry point's two limits.
     const size_t need = rmsnorm_bwd_workspace_bytes(T, D);
     if (need == 0) {
         // T == 0 (nothing to do) or an invalid shape: the regular entry point
@@ -61,11 +101,13 @@ extern "C" int rmsnorm_bwd_noalloc(const rmsn_bf16* g, int64_t ldg, const rmsn_b
         return rmsnorm_bwd(g, ldg, x, ldx, w, rstd, dx, lddx, dgamma, nullptr, 0, T, D, zero_centered_gamma,
                            stream);
     }
-    if (dgamma == nullptr) return RMSN_EINVAL;            // partials cannot be left in the shared array
+    const int st = rmsn::bwd_check_args(g, ldg, x, ldx, w, rstd, dx, lddx, dgamma, T, D);
+    if (st != RMSN_OK) return st;
+    if (dgamma == nullptr) return RMSN_EINVAL;                     // partials cannot be left in the shared array
     if (need > RMSN_NOALLOC_SCRATCH_BYTES) return RMSN_EWORKSPACE;  // problem too large for the array
     void* scratch = nullptr;
-    const int st = rmsn::scratch_address(&scratch);
-    if (st != RMSN_OK) return st;
+    const int sa = rmsn::scratch_address(&scratch);
+    if (sa != RMSN_OK) return sa;
     return rmsnorm_bwd(g, ldg, x, ldx, w, rstd, dx, lddx, dgamma, scratch, RMSN_NOALLOC_SCRATCH_BYTES, T, D,
                        zero_centered_gamma, stream);
 }

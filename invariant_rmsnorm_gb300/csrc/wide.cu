@@ -26,6 +26,10 @@ cudaError_t launch_wide_bwd(int m, const BwdArgs& a, const RowCfg& c, cudaStream
         case kResidual: return bwd_dispatch<kResidual>(a, c, st);
         case kGated: return bwd_dispatch<kGated>(a, c, st);
         case kGated | kFlagSigmoid: return bwd_dispatch<kGated | kFlagSigmoid>(a, c, st);
+        case kPlain | kFlagRecompute: return bwd_dispatch<kPlain | kFlagRecompute>(a, c, st);
+        case kResidual | kFlagRecompute: return bwd_dispatch<kResidual | kFlagRecompute>(a, c, st);
+        case kGated | kFlagRecompute: return bwd_dispatch<kGated | kFlagRecompute>(a, c, st);
+        case kGated | kFlagSigmoid | kFlagRecompute: return bwd_dispatch<kGated | kFlagSigmoid | kFlagRecompute>(a, c, st);
         case kFusedAdd: return bwd_dispatch<kFusedAdd>(a, c, st);
         case kFusedAddNoGres: return bwd_dispatch<kFusedAddNoGres>(a, c, st);
         default: break;

@@ -28,6 +28,10 @@ cudaError_t launch_wide_bwd_f16(int m, const BwdArgs& a, const RowCfg& c, cudaSt
         case kResidual | H: return bwd_dispatch<kResidual | H>(a, c, st);
         case kGated | H: return bwd_dispatch<kGated | H>(a, c, st);
         case kGated | kFlagSigmoid | H: return bwd_dispatch<kGated | kFlagSigmoid | H>(a, c, st);
+        case kPlain | kFlagRecompute | H: return bwd_dispatch<kPlain | kFlagRecompute | H>(a, c, st);
+        case kResidual | kFlagRecompute | H: return bwd_dispatch<kResidual | kFlagRecompute | H>(a, c, st);
+        case kGated | kFlagRecompute | H: return bwd_dispatch<kGated | kFlagRecompute | H>(a, c, st);
+        case kGated | kFlagSigmoid | kFlagRecompute | H: return bwd_dispatch<kGated | kFlagSigmoid | kFlagRecompute | H>(a, c, st);
         case kFusedAdd | H: return bwd_dispatch<kFusedAdd | H>(a, c, st);
         case kFusedAddNoGres | H: return bwd_dispatch<kFusedAddNoGres | H>(a, c, st);
         default: break;

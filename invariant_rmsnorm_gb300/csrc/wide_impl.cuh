@@ -89,6 +89,12 @@
 #ifndef RMSN_BWD_HOLD_WIDE
 #define RMSN_BWD_HOLD_WIDE 1  // VPT 4 at 512 threads: re-read staged operands after the reduction
 #endif
+#ifndef RMSN_BWD_GATE_KEEP
+#define RMSN_BWD_GATE_KEEP 0
+#endif
+#ifndef RMSN_BWD_DIET_224
+#define RMSN_BWD_DIET_224 1  // VPT 4 at 224 threads, modes streaming 3-4 operands: HOLD and WL1 as well
+#endif
 #ifndef RMSN_BWD_WL1_WIDE
 #define RMSN_BWD_WL1_WIDE 1  // VPT 4 at 512 threads: weights from L1 where used
 #endif
@@ -480,6 +486,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr int NIN = bwd_inputs(MODE);
     constexpr int R = bwd_rows<VPT, MAXT>();
     constexpr int NWMAX = MAXT / 32;
+    constexpr bool RY = is_recompute(MODE);  // also write y (a.y is then not null)
     // Rows per weight-gradient chunk: kWideChunkRows, or with VC the chunk the
     // host chose for T (a.chunk, which R divides); VC kernels step through
     // their rows without dividing by it.
@@ -493,8 +500,13 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // from L1 where they are used instead of keeping them in registers.
     // Measured at D=16384: 783 -> 667 us per 32768 rows; at 256 threads
     // (D <= 8192) both cost more than they save.
-    constexpr bool HOLD = VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE;
-    constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
+    constexpr bool V4_224_DIET = VPT == 4 && MAXT == 224 && M != kPlain && RMSN_BWD_DIET_224;
+    // GK (gated): the gate and its derivative are evaluated once, before the
+    // row reduction, and g q(z), g q'(z) are kept across it, instead of
+    // evaluating the gate again after it.
+    constexpr bool GK = M == kGated && RMSN_BWD_GATE_KEEP;
+    constexpr bool HOLD = (VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE) || V4_224_DIET;
+    constexpr bool WL1 = (VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE) || V4_224_DIET;
     // Element pairs through the packed fp32 instructions (same bits as the
     // scalar loops), where they measured faster: every site of the two-vector
     // kernels on 128 and on 512 threads (131072 x 2048: 282 -> 259 us;
@@ -604,8 +616,9 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         float gw[R][VPT][8];  // g*w_eff   (gated: g*q(z)*w_eff)
         float xs[R][VPT][8];  // x
         float gx[R][VPT][8];  // g*x       (gated: g*q(z)*x)
-        float tz[R][VPT][8];  // residual: g_res; gated: z; fused add: res
-        float g0[R][VPT][8];  // gated: g
+        float tz[R][VPT][8];  // residual: g_res; gated: z, then q(z); fused add: res
+        float g0[R][VPT][8];  // gated: g q'(z)
+        float gq[R][VPT][8];  // gated with GK: g q(z), kept across the row reduction
         float rr[R];
         float sp[R];          // this thread's part of s = sum g x w_eff (gated: g q x w_eff)
         uint4 gv[R][VPT], xv[R][VPT], tv[R][VPT], fv[R][VPT];  // fv: fused add's g_res
@@ -657,8 +670,16 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         if (M == kGated) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                g0[r][j][e] = gf[e];
-                                gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));  // g*q(z)
+                                if (RMSN_BWD_LEAN && !GK) {
+                                    gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));  // g*q(z)
+                                } else {  // kept: g*q'(z) in g0, q(z) in tz, g*q(z) in gq
+                                    float q, dq;
+                                    gate_eval<SIG>(tz[r][j][e], q, dq);
+                                    g0[r][j][e] = fmul(gf[e], dq);
+                                    tz[r][j][e] = q;
+                                    gf[e] = fmul(gf[e], q);
+                                    gq[r][j][e] = gf[e];
+                                }
                             }
                         }
                         if constexpr (X2P1) {
@@ -717,19 +738,30 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
                         }
                         if (RMSN_BWD_LEAN) {
-                            // Recompute the phase-1 products from the packed row (same bits).
+                            // Recompute the phase-1 products from the packed row (same bits);
+                            // GK: from the kept g*q(z) and the packed x.
                             float gf[8];
-                            unpack_act<F16>(gv[r][j], gf);
-                            norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
-                            if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
-                            if constexpr (X2RC) {
-                                if (M == kGated) {
+                            if (GK) {
 #pragma unroll
-                                    for (int e = 0; e < 8; ++e) {
-                                        g0[r][j][e] = gf[e];
-                                        gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));
-                                    }
+                                for (int e = 0; e < 8; ++e) gf[e] = gq[r][j][e];
+                                norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
+                            } else {
+                                unpack_act<F16>(gv[r][j], gf);
+                                norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
+                                if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
+                            }
+                            if (M == kGated && !GK) {
+                                // The gate and its derivative, once: g*q'(z) in g0, q(z) in tz.
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    float q, dq;
+                                    gate_eval<SIG>(tz[r][j][e], q, dq);
+                                    g0[r][j][e] = fmul(gf[e], dq);
+                                    tz[r][j][e] = q;
+                                    gf[e] = fmul(gf[e], q);
                                 }
+                            }
+                            if constexpr (X2RC) {
 #pragma unroll
                                 for (int e = 0; e < 8; e += 2) {
                                     const float2 gw2 = fmul2(pair(gf, e), pair(wj, e));
@@ -742,10 +774,6 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             } else {
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
-                                    if (M == kGated) {
-                                        g0[r][j][e] = gf[e];
-                                        gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));
-                                    }
                                     gw[r][j][e] = fmul(gf[e], wj[e]);
                                     gx[r][j][e] = fmul(gf[e], xs[r][j][e]);
                                 }
@@ -780,15 +808,13 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         st_global_cs(dxrow + 8 * v, pack_act<F16>(o));
                         if (M == kGated) {
                             float dzv[8], yv[8];
+                            // dz = (g q'(z)) u and y = u q(z), u = (x r) w_eff.
                             if constexpr (X2OUT) {
-                                float q[8], dq[8];
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) gate_eval<SIG>(tz[r][j][e], q[e], dq[e]);
 #pragma unroll
                                 for (int e = 0; e < 8; e += 2) {
                                     const float2 u = fmul2(fmul2(pair(xs[r][j], e), both(r1)), pair(wj, e));
-                                    const float2 dz2 = fmul2(fmul2(pair(g0[r][j], e), u), pair(dq, e));
-                                    const float2 y2 = fmul2(u, pair(q, e));
+                                    const float2 dz2 = fmul2(pair(g0[r][j], e), u);
+                                    const float2 y2 = fmul2(u, pair(tz[r][j], e));
                                     dzv[e] = dz2.x;
                                     dzv[e + 1] = dz2.y;
                                     yv[e] = y2.x;
@@ -797,16 +823,14 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             } else {
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
-                                    float q, dq;
-                                    gate_eval<SIG>(tz[r][j][e], q, dq);
                                     const float u = fmul(fmul(xs[r][j][e], r1), wj[e]);
-                                    dzv[e] = fmul(fmul(g0[r][j][e], u), dq);
-                                    yv[e] = fmul(u, q);
+                                    dzv[e] = fmul(g0[r][j][e], u);
+                                    yv[e] = fmul(u, tz[r][j][e]);
                                 }
                             }
                             st_global_cs(a.dz + row * a.lddz + 8 * v, pack_act<F16>(dzv));
-                            if (a.y) st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
-                        } else if (a.y) {
+                            if constexpr (RY) st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
+                        } else if constexpr (RY) {
                             // The forward output again, from the saved rstd: same operations,
                             // same bits as the forward's y.
                             float yv[8];

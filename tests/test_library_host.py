@@ -116,6 +116,32 @@ def test_host_validation_rejects_before_launch(lib):
     assert lib.rmsnorm_device_error(None, 0) == -1
 
 
+def test_noalloc_checks_arguments_in_the_backward_order(lib):
+    """rmsnorm_bwd_noalloc fails with the status rmsnorm_bwd gives for the same
+    bad argument, also when the problem is too large for its array; a NULL
+    dgamma and then the array's size come after those checks. Fake addresses:
+    every case fails before the device is touched."""
+    A = 1 << 20
+    big_T, D = 32769, 8192                      # one chunk past the 32 MiB array
+    assert rn.rmsnorm_bwd_workspace_bytes(big_T, D) > 32 << 20
+    assert rn.rmsnorm_bwd_workspace_bytes(32768, D) == 32 << 20
+
+    def call(g=A, x=A, w=A, r=A, dx=A, ld=D, dg=A, T=big_T):
+        return lib.rmsnorm_bwd_noalloc(g, ld, x, ld, w, r, dx, ld, dg, T, D, 0, None)
+
+    def ref(g=A, x=A, w=A, r=A, dx=A, ld=D, dg=A, T=big_T):
+        return lib.rmsnorm_bwd(g, ld, x, ld, w, r, dx, ld, dg, A, 1 << 40, T, D, 0, None)
+
+    for bad in (dict(g=0), dict(x=A + 2), dict(dx=0), dict(w=A + 4), dict(r=0), dict(dg=A + 8), dict(ld=D + 4),
+                dict(ld=D - 8), dict(T=-1)):
+        st = call(**bad)
+        assert st in (-1, -2) and st == ref(**bad), bad
+    assert call(dg=0) == -1                      # NULL dgamma: the partials cannot stay in the shared array
+    assert call() == -5                          # valid arguments, too large for the array
+    assert call(T=0) == 0 and call(g=0, x=0, w=0, r=0, dx=0, dg=0, T=0) == 0
+    assert lib.rmsnorm_bwd_noalloc(A, 8, A, 8, A, A, A, 8, A, 4, 7, 0, None) == -3  # D not a multiple of 8
+
+
 def test_ex_options_are_validated_on_the_host(lib):
     """Unknown activation formats and gates are rejected before anything else;
     known ones reach the ordinary validation (here: a null input)."""
@@ -166,6 +192,22 @@ def test_workspace_size_is_not_monotone_and_the_max_query_covers_it(lib):
     for T, D in ((100000, 2048), (70000, 128), (50000, 8192), (200000, 4096)):
         assert qmax(T, D) == q(T, D)  # the size grows with T here
     assert qmax(0, 4096) == 0 and qmax(100, 7) == 0
+
+
+def test_workspace_max_closed_form_matches_scan(lib):
+    """The max query is a closed form, not a scan: for every T_max up to 131072
+    (past the last row count whose chunks are shortened) it equals the running
+    maximum of the per-T size, at widths inside and at the edges of the band
+    where chunks are shortened; far beyond it, it is the per-T size."""
+    q, qmax = rn.rmsnorm_bwd_workspace_bytes, rn.rmsnorm_bwd_workspace_bytes_max
+    for D in (2056, 4096, 7168):
+        run = 0
+        for t in range(1, 131073):
+            run = max(run, q(t, D))
+            assert qmax(t, D) == run, (t, D)
+    for D in (2048, 4096, 7168, 7176):
+        for T in (10 ** 6, 10 ** 9, 2 ** 31 - 1):
+            assert qmax(T, D) == q(T, D)
 
 
 @pytest.mark.parametrize("T,D", [(1, 128), (100, 64), (32768, 4096), (4097, 4096), (70000, 8)])

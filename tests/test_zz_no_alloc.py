@@ -6,9 +6,10 @@ after start-up — so it keeps the weight-gradient scratch in a fixed array in
 the library's device image instead of a caller workspace. This test calls it
 through the C ABI and checks that its dx and dgamma equal those of the regular
 rmsnorm_bwd (caller workspace) on the same inputs, bit for bit, on consecutive
-calls of different sizes (including one that fills the whole array and one
-that follows it and finds its leftovers), and that a problem too large for the
-array is refused. This file is collected last so that a failure here cannot
+calls of different sizes: one that fills the whole array exactly
+(T = 32768, D = 8192: 1024 chunks of 32 rows x 8192 x 4 bytes = 32 MiB), one
+that uses part of it, and smaller ones that follow them and find their
+leftovers. A problem one chunk past the array is refused. This file is collected last so that a failure here cannot
 hide the results of the other GPU tests.
 """
 from __future__ import annotations
@@ -38,9 +39,11 @@ LIMIT = 32 << 20  # RMSN_NOALLOC_SCRATCH_BYTES
 
 
 def test_noalloc_backward_matches_workspace_backward():
-    # T = 32768 at D = 4096 (27-row chunks: 1214 partial rows, 19.9 MB of the 32 MiB array)
+    # T = 32768 at D = 8192 fills the array exactly; at D = 4096 (27-row chunks:
+    # 1214 partial rows) it takes 19.9 MB of it.
+    assert rn.workspace_bytes(32768, 8192) == LIMIT
     assert 16 << 20 < rn.workspace_bytes(32768, 4096) <= LIMIT
-    cases = [(4096, 4096, 1, False), (32768, 4096, 2, False), (100, 2048, 3, True)]
+    cases = [(4096, 4096, 1, False), (32768, 8192, 4, False), (32768, 4096, 2, False), (100, 2048, 3, True)]
     for T, D, seed, zc in cases:
         g, x, w, rstd = _inputs(T, D, seed, zc)
         dx_ref = torch.empty_like(x)
@@ -68,3 +71,13 @@ def test_noalloc_refuses_problems_larger_than_its_array():
     with pytest.raises(rn.RmsNormError) as err:
         rn.rmsnorm_bwd_noalloc(x[:8], x[:8], w, rstd[:8], x[:8].clone(), None, False)
     assert err.value.status == -1
+    # one chunk past the array at D = 8192
+    D, T = 8192, 32769
+    assert rn.workspace_bytes(T, D) == LIMIT + D * 4
+    x = torch.zeros((T, D), dtype=torch.bfloat16, device=DEV)
+    w = torch.ones(D, device=DEV)
+    rstd = torch.ones(T, device=DEV)
+    dg = torch.empty(D, device=DEV)
+    with pytest.raises(rn.RmsNormError) as err:
+        rn.rmsnorm_bwd_noalloc(x, x, w, rstd, torch.empty_like(x), dg, False)
+    assert err.value.status == -5
