@@ -280,8 +280,14 @@ def run_ours(args):
     b2b = _time_gbs(lambda: rn.rmsnorm_residual_bwd(wl.g, wl.x, wl.w, rstd, wl.g_res, dx, None, ws, False,
                                                     stream=stream),
                     bwd_pass1_bytes(T, D), 200, stream)
+    # The forward the same way: its roofline figure comes from this run, not
+    # from the sampled steps' events (which cost it its early launch too).
+    f2f = _time_gbs(lambda: rn.rmsnorm_residual_fwd(wl.x, wl.w, y, rstd, xc, EPS, False, stream=stream),
+                    fwd_bytes(T, D), 200, stream)
 
     cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        extra["gated_262144x128_cpu_baseline"] = cpu_gated_sample()
     peak, peak_kind = peaks()
     bwd_gbs = bwd_pass1_bytes(T, D) / (bwd_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
@@ -295,14 +301,19 @@ def run_ours(args):
             "dtype": "f32", "data": "synthetic",
             "config": residual_config(world),
             "pct_of_peak": round(100.0 * value / (world * peak), 2),
+            "rows_per_s": round(world * T / (ms_per_step * 1e-3)),
             "kernels_ms": {"fwd": round(fwd_ms, 5), "bwd_pass1": round(bwd_ms, 5), "dgamma_pass2": round(red_ms, 5),
-                           "sampled_steps": len(evs)},
+                           "sampled_steps": len(evs),
+                           "note": "events between the kernels of every 16th step; they delay each kernel's "
+                                   "early launch, so these read slower than the back-to-back figures"},
             "roofline": {"kernel": "wide_bwd_kernel (residual, pass 1)", "bound": "hbm",
                          "achieved": round(bwd_gbs, 2), "peak": peak, "unit": "GB/s",
                          "frac": round(bwd_gbs / peak, 4), "peak_kind": peak_kind,
                          "traffic": traffic, "algorithmic_bytes_per_launch": bwd_pass1_bytes(T, D)},
-            "fwd_roofline": {"achieved": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9, 2), "peak": peak,
-                             "frac": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9 / peak, 4)},
+            "fwd_roofline": {"kernel": "wide_fwd_kernel (residual)", "achieved": f2f["gbs"], "peak": peak,
+                             "frac": round(f2f["gbs"] / peak, 4), "us": round(f2f["ms"] * 1e3, 2),
+                             "how": "200 launches back to back on the stream, CUDA events around the run",
+                             "sampled_steps_gbs": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9, 2)},
             "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
                     "how": "rmsnorm_residual_step_host: 4096-row slabs, copies overlapped with the kernels inside the library",
@@ -378,6 +389,11 @@ def run_gated(args):
     value = world * nbytes / (ms_per_step * 1e-3) / 1e9
     peak, peak_kind = peaks()
     bwd_bytes = T * (10 * D + 4)
+    # each kernel launched back to back on its own (no events between kernels)
+    b2b = _time_gbs(lambda: rn.rmsnorm_gated_bwd(g.g, g.x, g.z, g.w, rstd, dx, dz, None, ws, True, stream=stream),
+                    bwd_bytes, 200, stream)
+    f2f = _time_gbs(lambda: rn.rmsnorm_gated_fwd(g.x, g.z, g.w, y, rstd, EPS, True, stream=stream),
+                    T * (6 * D + 4), 200, stream)
     if rank == 0:
         print(json.dumps({
             "metric": "gated RMSNorm fwd+bwd HBM GB/s at 262144 x 128, bf16", "value": round(value, 2),
@@ -388,12 +404,16 @@ def run_gated(args):
                        "gate": "silu", "eps": EPS, "parallelism": f"replicas x{world}",
                        "l2": "inputs 0.54 GB per step, larger than L2; no flush"},
             "pct_of_peak": round(100.0 * value / (world * peak), 2),
+            "rows_per_s": round(world * T / (ms_per_step * 1e-3)),
             "kernels_ms": {"fwd": round(kms[0], 5), "bwd_pass1": round(kms[1], 5), "dgamma_pass2": round(kms[2], 5),
                            "sampled_steps": len(evs)},
             "roofline": {"kernel": "narrow_bwd_kernel (gated, pass 1)", "bound": "hbm",
-                         "achieved": round(bwd_bytes / (kms[1] * 1e-3) / 1e9, 2), "peak": peak, "unit": "GB/s",
-                         "frac": round(bwd_bytes / (kms[1] * 1e-3) / 1e9 / peak, 4), "peak_kind": peak_kind,
+                         "achieved": b2b["gbs"], "peak": peak, "unit": "GB/s",
+                         "frac": round(b2b["gbs"] / peak, 4), "peak_kind": peak_kind, "us": round(b2b["ms"] * 1e3, 2),
+                         "how": "200 launches back to back on the stream, CUDA events around the run",
                          "traffic": None, "algorithmic_bytes_per_launch": bwd_bytes},
+            "fwd_roofline": {"kernel": "narrow_fwd_kernel (gated)", "achieved": f2f["gbs"], "peak": peak,
+                             "frac": round(f2f["gbs"] / peak, 4), "us": round(f2f["ms"] * 1e3, 2)},
             "gpu_launches": 3 * args.steps, "clocks": clocks}))
     barrier()
 
@@ -456,48 +476,84 @@ def run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream, steps, slab=4096):
 
 
 def side_measurements(rn, synth, dev, stream, reps=50):
+    """Side lines (not part of `value`): other variants and the pages' other
+    shapes, each timed back to back on the stream with inputs resident. Every
+    entry gives ms per call, GB/s of algorithmic bytes, the fraction of the
+    measured HBM peak and rows/s."""
     import torch
+    peak, _ = peaks()
     res = {}
+
+    def rec(name, fn, T, per_row):
+        r = _time_gbs(fn, T * per_row, reps, stream)
+        r["frac"] = round(r["gbs"] / peak, 4)
+        r["rows_per_s"] = round(T / (r["ms"] * 1e-3))
+        r["T"], r["bytes_per_row"] = T, per_row
+        res[name] = r
+
+    def buffers(T, D):
+        return (torch.empty(T, device=dev), torch.empty(D, device=dev),
+                torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev))
+
     # plain fwd+bwd, same shape (the metric's literal op): 10*D + 8 bytes per row
     T, D = T_ROWS, D_COLS
     wl = synth.tiny_plain(dev, seed=3, T=T, D=D)
     y, dx = torch.empty_like(wl.x), torch.empty_like(wl.x)
-    r, dg = torch.empty(T, device=dev), torch.empty(D, device=dev)
-    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+    r, dg, ws = buffers(T, D)
 
     def plain():
         rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, False, stream=stream)
         rn.rmsnorm_bwd(wl.g, wl.x, wl.w, r, dx, dg, ws, False, stream=stream)
-    res["plain_fwd_bwd_gbs"] = _time_gbs(plain, T * (10 * D + 8), reps, stream)
-    del wl, y, dx
-    # gated, 262144 x 128: 16*D + 8 bytes per row
-    g = synth.gated(dev, seed=4)
-    T, D = g.T, g.D
-    y, dx, dz = torch.empty_like(g.x), torch.empty_like(g.x), torch.empty_like(g.x)
-    r, dw = torch.empty(T, device=dev), torch.empty(D, device=dev)
-    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+    rec("plain_fwd_bwd_gbs", plain, T, 10 * D + 8)
+    del wl, y, dx, r, dg, ws
+    # the residual step at the pages' two larger row counts (D = 4096): 14*D + 8 bytes per row
+    for T in (131072, 262144):
+        wl = synth.residual(dev, seed=11, T=T, D=D)
+        y, xc, dx = torch.empty_like(wl.x), torch.empty_like(wl.x), torch.empty_like(wl.x)
+        r, dg, ws = buffers(T, D)
 
-    def gated():
-        rn.rmsnorm_gated_fwd(g.x, g.z, g.w, y, r, EPS, True, stream=stream)
-        rn.rmsnorm_gated_bwd(g.g, g.x, g.z, g.w, r, dx, dz, dw, ws, True, stream=stream)
-    res["gated_262144x128_fwd_bwd_gbs"] = _time_gbs(gated, T * (16 * D + 8), reps, stream)
-    del g, y, dx, dz
-    # fused add + norm at the decoder shape, 32768 x 2048: 18*D + 8 bytes per row
-    # (x, res in; y, res_out, rstd out; g, x, res, g_res, rstd in; dh out)
-    T, D = 32768, 2048
-    x = synth.normal_bf16((T, D), 5, dev)
-    rs = synth.normal_bf16((T, D), 6, dev, std=4.0)
-    gg = synth.normal_bf16((T, D), 7, dev)
-    gr = synth.normal_bf16((T, D), 8, dev)
-    w = synth.gamma_f32(D, 9, dev)
-    y, ro, dh = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
-    r, dw = torch.empty(T, device=dev), torch.empty(D, device=dev)
-    ws = torch.empty(rn.workspace_bytes(T, D), dtype=torch.uint8, device=dev)
+        def step():
+            rn.rmsnorm_residual_fwd(wl.x, wl.w, y, r, xc, EPS, False, stream=stream)
+            rn.rmsnorm_residual_bwd(wl.g, wl.x, wl.w, r, wl.g_res, dx, dg, ws, False, stream=stream)
+        rec(f"residual_{T}x{D}_fwd_bwd_gbs", step, T, 14 * D + 8)
+        del wl, y, xc, dx, r, dg, ws
+    # gated: Qwen3-Next 262144 x 128, and wide rows: 16*D + 8 bytes per row
+    for T, D in ((262144, 128), (32768, 7168), (32768, 8192)):
+        g = synth.gated(dev, seed=4, T=T, D=D)
+        y, dx, dz = torch.empty_like(g.x), torch.empty_like(g.x), torch.empty_like(g.x)
+        r, dw, ws = buffers(T, D)
 
-    def fused():
-        rn.rmsnorm_fused_add_fwd(x, rs, w, y, r, ro, EPS, False, stream=stream)
-        rn.rmsnorm_fused_add_bwd(gg, x, rs, w, r, gr, dh, dw, ws, False, stream=stream)
-    res["fused_add_32768x2048_fwd_bwd_gbs"] = _time_gbs(fused, T * (18 * D + 8), reps, stream)
+        def gated():
+            rn.rmsnorm_gated_fwd(g.x, g.z, g.w, y, r, EPS, True, stream=stream)
+            rn.rmsnorm_gated_bwd(g.g, g.x, g.z, g.w, r, dx, dz, dw, ws, True, stream=stream)
+        rec(f"gated_{T}x{D}_fwd_bwd_gbs", gated, T, 16 * D + 8)
+        del g, y, dx, dz, r, dw, ws
+    # fused add + norm: 18*D + 8 bytes per row (x, res in; y, res_out, rstd out;
+    # g, x, res, g_res, rstd in; dh out); the decoder shape 32768 x 2048 and wide rows
+    for T, D in ((32768, 2048), (32768, 7168), (32768, 8192)):
+        x = synth.normal_bf16((T, D), 5, dev)
+        rs = synth.normal_bf16((T, D), 6, dev, std=4.0)
+        gg = synth.normal_bf16((T, D), 7, dev)
+        gr = synth.normal_bf16((T, D), 8, dev)
+        w = synth.gamma_f32(D, 9, dev)
+        y, ro, dh = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+        r, dw, ws = buffers(T, D)
+
+        def fused():
+            rn.rmsnorm_fused_add_fwd(x, rs, w, y, r, ro, EPS, False, stream=stream)
+            rn.rmsnorm_fused_add_bwd(gg, x, rs, w, r, gr, dh, dw, ws, False, stream=stream)
+        rec(f"fused_add_{T}x{D}_fwd_bwd_gbs", fused, T, 18 * D + 8)
+        del x, rs, gg, gr, w, y, ro, dh, r, dw, ws
+    # the widest rows: plain backward (pass 1 and 2) at 32768 x 16384, 6*D + 4 bytes per row
+    T, D = 32768, 16384
+    wl = synth.tiny_plain(dev, seed=12, T=T, D=D)
+    y, dx = torch.empty_like(wl.x), torch.empty_like(wl.x)
+    r, dg, ws = buffers(T, D)
+    rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, False, stream=stream)
+    rec(f"plain_bwd_{T}x{D}_gbs", lambda: rn.rmsnorm_bwd(wl.g, wl.x, wl.w, r, dx, dg, ws, False, stream=stream),
+        T, 6 * D + 4)
+    rec(f"plain_fwd_{T}x{D}_gbs", lambda: rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, False, stream=stream), T, 4 * D + 4)
+    del wl, y, dx, r, dg, ws
     return res
 
 
@@ -549,6 +605,33 @@ def cpu_baseline_sample(target_s=10.0):
     return {"value": round(n * step_bytes(rows, D_COLS) / dt / 1e9, 4), "unit": "GB/s",
             "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} repetitions of {rows} rows x {D_COLS} (residual fwd+bwd, float64 C oracle), {dt:.1f} s"}
+
+
+def cpu_gated_sample(target_s=5.0, rows=8192):
+    """The oracle on the gated step (forward, backward with dx, dz and the weight
+    gradient) on repeated row samples of the 262144 x 128 Qwen3-Next workload."""
+    import numpy as np
+
+    import oracle
+    from invariant_rmsnorm_gb300 import synth
+    g = synth.gated("cpu", seed=0, T=rows)
+    f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+    x, z, w, gg = f(g.x), f(g.z), f(g.w), f(g.g)
+
+    def step():
+        _, r = oracle.gated_fwd(x, z, w, EPS, True)
+        oracle.gated_bwd(gg, x, z, w, r, True)
+    step()
+    t0 = time.perf_counter()
+    n = 0
+    while time.perf_counter() - t0 < target_s:
+        step()
+        n += 1
+    dt = time.perf_counter() - t0
+    D = g.D
+    return {"value": round(n * rows * (16 * D + 8) / dt / 1e9, 4), "unit": "GB/s",
+            "rows_per_s": round(n * rows / dt), "cores": oracle.num_threads(), "kind": "oracle",
+            "sample": f"{n} repetitions of {rows} rows x {D} (gated fwd+bwd, float64 C oracle), {dt:.1f} s"}
 
 
 def run_reference(args):
