@@ -265,15 +265,22 @@ def run_ours(args):
     ms_per_step = total_ms / args.steps
     value = world * step_bytes(T, D) / (ms_per_step * 1e-3) / 1e9
 
-    # End to end through the public API: every step copies its inputs from
-    # pinned host memory, runs the step, and copies every output back.
-    e2e_ms_serial, e2e_ms, h2d, d2h, e2e_same_bits = run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream,
-                                                             max(3, min(20, args.steps)))
-    e2e_value = world * step_bytes(T, D) / (e2e_ms * 1e-3) / 1e9
-    e2e_serial_value = world * step_bytes(T, D) / (e2e_ms_serial * 1e-3) / 1e9
-
-    # side measurements (not part of `value`): plain and gated fwd+bwd
-    extra = side_measurements(rn, synth, dev, stream) if rank == 0 else {}
+    e2e = None
+    extra = {}
+    if not args.main_only:
+        # End to end through the public API: every step copies its inputs from
+        # pinned host memory, runs the step, and copies every output back.
+        e2e_ms_serial, e2e_ms, h2d, d2h, e2e_same_bits = run_e2e(rn, wl, y, xc, dx, rstd, dg, ws, T, D, stream,
+                                                                 max(3, min(20, args.steps)))
+        e2e_value = world * step_bytes(T, D) / (e2e_ms * 1e-3) / 1e9
+        e2e_serial_value = world * step_bytes(T, D) / (e2e_ms_serial * 1e-3) / 1e9
+        e2e = {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
+               "how": "rmsnorm_residual_step_host: 4096-row slabs, copies overlapped with the kernels inside the library",
+               "bitwise_equal_to_unsliced_step": e2e_same_bits,
+               "serial_value": round(e2e_serial_value, 2), "serial_ms_per_step": round(e2e_ms_serial, 4)}
+        # side measurements (not part of `value`): other variants and shapes
+        extra = side_measurements(rn, synth, dev, stream) if rank == 0 else {}
     # The dominant kernel launched back to back on its own (each launch chained
     # to the previous one by programmatic dependent launch, as in the step):
     # the sampled events above cost it its early launch, this does not.
@@ -285,8 +292,9 @@ def run_ours(args):
     f2f = _time_gbs(lambda: rn.rmsnorm_residual_fwd(wl.x, wl.w, y, rstd, xc, EPS, False, stream=stream),
                     fwd_bytes(T, D), 200, stream)
 
-    cpu = cpu_baseline_sample() if (rank == 0 and world == 1 and not args.no_cpu_baseline) else None
-    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+    with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and not args.main_only
+    cpu = cpu_baseline_sample() if with_cpu else None
+    if with_cpu:
         extra["gated_262144x128_cpu_baseline"] = cpu_gated_sample()
     peak, peak_kind = peaks()
     bwd_gbs = bwd_pass1_bytes(T, D) / (bwd_ms * 1e-3) / 1e9
@@ -314,11 +322,7 @@ def run_ours(args):
                              "frac": round(f2f["gbs"] / peak, 4), "us": round(f2f["ms"] * 1e3, 2),
                              "how": "200 launches back to back on the stream, CUDA events around the run",
                              "sampled_steps_gbs": round(fwd_bytes(T, D) / (fwd_ms * 1e-3) / 1e9, 2)},
-            "e2e": {"value": round(e2e_value, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_ms, 4),
-                    "how": "rmsnorm_residual_step_host: 4096-row slabs, copies overlapped with the kernels inside the library",
-                    "bitwise_equal_to_unsliced_step": e2e_same_bits,
-                    "serial_value": round(e2e_serial_value, 2), "serial_ms_per_step": round(e2e_ms_serial, 4)},
+            "e2e": e2e,
             "gpu_launches": 3 * args.steps,
             "clocks": clocks,
             "bwd_pass1_back_to_back": {"us": round(b2b["ms"] * 1e3, 2), "gbs": b2b["gbs"],
@@ -675,6 +679,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true", help="skip the timed CPU-oracle sample")
+    ap.add_argument("--main-only", action="store_true",
+                    help="the timed steps and the back-to-back kernel runs only: no end-to-end run, side lines or "
+                         "CPU samples (a small, fixed driver for profiler captures; the line then has no e2e)")
     ap.add_argument("--workload", choices=("residual", "gated"), default="residual",
                     help="residual: the benchmark line (default); gated: the 262144 x 128 gated step, device "
                          "timing only")

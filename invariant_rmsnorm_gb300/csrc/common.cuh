@@ -140,30 +140,19 @@ __device__ __forceinline__ int named_bar_and(int id, int nthreads, int pred) {
 // Bounded wait for the phase with parity `parity` to complete. Returns false if
 // `limit_ns` (the kernels use kWaitTimeoutNs) of global time elapsed without
 // completion.
-#ifndef RMSN_WAIT_HINT_NS
-#define RMSN_WAIT_HINT_NS 0  // suspend-time hint of each try_wait (0: the hardware's default)
-#endif
 __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
                                           unsigned long long limit_ns = kWaitTimeoutNs) {
     const uint32_t addr = smem_u32(bar);
     uint32_t done = 0;
     unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
-#if RMSN_WAIT_HINT_NS
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2, %3;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done) : "r"(addr), "r"(parity), "n"(RMSN_WAIT_HINT_NS) : "memory");
-#else
         asm volatile(
             "{\n\t.reg .pred p;\n\t"
             "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
             "selp.u32 %0, 1, 0, p;\n\t}"
             : "=r"(done) : "r"(addr), "r"(parity) : "memory");
-#endif
         if (done) return true;
-        if (RMSN_WAIT_HINT_NS || (it & 255u) == 0u) {  // with a hint, every try sleeps: check each time
+        if ((it & 255u) == 0u) {
             const unsigned long long now = global_timer_ns();
             if (it == 0) t0 = now;
             else if (now - t0 > limit_ns) return false;

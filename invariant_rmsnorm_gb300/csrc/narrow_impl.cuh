@@ -50,15 +50,6 @@
 #ifndef RMSN_NARROW_BWD_MINB
 #define RMSN_NARROW_BWD_MINB 3  // backward CTAs that must fit on one SM (register budget)
 #endif
-#ifndef RMSN_NARROW_GATED_X2
-#define RMSN_NARROW_GATED_X2 0
-#endif
-#ifndef RMSN_NARROW_COMB_BUFS
-#define RMSN_NARROW_COMB_BUFS 2  // chunk-combine buffers of the backward (1: one more barrier per chunk)
-#endif
-#ifndef RMSN_NARROW_FWD_X2
-#define RMSN_NARROW_FWD_X2 0
-#endif
 
 namespace rmsn {
 
@@ -179,7 +170,6 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
     constexpr int P = narrow_pass_rows<G>();
     constexpr int RS = narrow_fwd_stage_rows<G>();
     constexpr int NP = RS / P;
-    constexpr bool FX2 = RMSN_F32X2 && RMSN_NARROW_FWD_X2;  // gated output products in packed pairs
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -270,17 +260,8 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 if (lane_valid) {
                     float o[8];
                     if (M == kGated) {
-                        if constexpr (FX2) {
 #pragma unroll
-                            for (int e = 0; e < 8; e += 2) {
-                                const float2 o2 = fmul2(fmul2(fmul2(pair(f, e), both(r)), pair(we, e)), pair(q, e));
-                                o[e] = o2.x;
-                                o[e + 1] = o2.y;
-                            }
-                        } else {
-#pragma unroll
-                            for (int e = 0; e < 8; ++e) o[e] = fmul(fmul(fmul(f[e], r), we[e]), q[e]);
-                        }
+                        for (int e = 0; e < 8; ++e) o[e] = fmul(fmul(fmul(f[e], r), we[e]), q[e]);
                     } else if (M == kGatedHF) {
                         // HF convention: normalised value and weight multiply in bf16.
 #pragma unroll
@@ -323,7 +304,6 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
     constexpr int CN = narrow_chunk_rows<G>();
     constexpr int NSC = CN / RS;  // stages per chunk
     constexpr bool RY = is_recompute(MODE);  // also write y (a.y is then not null)
-    constexpr bool NX2 = RMSN_F32X2 && RMSN_NARROW_GATED_X2 && M == kGated;
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
     const int NV = D >> 3;
@@ -426,37 +406,18 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 float zf[8], q[8], dq[8];
                 unpack_act<F16>(tv, zf);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) gate_eval<SIG>(zf[e], q[e], dq[e]);
-#pragma unroll
-                for (int e = 0; e < 8; e += 2) {
-                    if constexpr (NX2) {
-                        const float2 d2 = fmul2(pair(gf, e), pair(dq, e)), g2 = fmul2(pair(gf, e), pair(q, e));
-                        gd[e] = d2.x; gd[e + 1] = d2.y;  // g q'(z)
-                        gf[e] = g2.x; gf[e + 1] = g2.y;  // g q(z)
-                    } else {
-                        gd[e] = fmul(gf[e], dq[e]);
-                        gd[e + 1] = fmul(gf[e + 1], dq[e + 1]);
-                        gf[e] = fmul(gf[e], q[e]);
-                        gf[e + 1] = fmul(gf[e + 1], q[e + 1]);
-                    }
+                for (int e = 0; e < 8; ++e) {
+                    gate_eval<SIG>(zf[e], q[e], dq[e]);
+                    gd[e] = fmul(gf[e], dq[e]);  // g q'(z)
+                    gf[e] = fmul(gf[e], q[e]);   // g q(z)
                 }
             }
             float gw[8];
             float sp = 0.0f;
-            if constexpr (NX2) {
 #pragma unroll
-                for (int e = 0; e < 8; e += 2) {  // products packed, s in ascending element order
-                    const float2 gw2 = fmul2(pair(gf, e), pair(we, e));
-                    gw[e] = gw2.x; gw[e + 1] = gw2.y;
-                    const float2 t2 = fmul2(gw2, pair(xf, e));
-                    sp = fadd(fadd(sp, t2.x), t2.y);
-                }
-            } else {
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    gw[e] = fmul(gf[e], we[e]);
-                    sp = fadd(sp, fmul(gw[e], xf[e]));
-                }
+            for (int e = 0; e < 8; ++e) {
+                gw[e] = fmul(gf[e], we[e]);
+                sp = fadd(sp, fmul(gw[e], xf[e]));
             }
             sp = group_sum<G>(sp);
             const float coef = fmul(div_by_d(fmul(fmul(r, r), r), D, a.inv_d_pow2), sp);
@@ -466,29 +427,12 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 if (M == kGated) {
                     // dx; dw term (g q) (x r); dz = (g q') u with u = (x r) w_eff; y = u q.
                     float dzv[8];
-                    if constexpr (NX2) {
-                        const float2 r2 = both(r), c2 = both(coef);
 #pragma unroll
-                        for (int e = 0; e < 8; e += 2) {  // products packed, their sums scalar
-                            const float2 p2 = fmul2(pair(gw, e), r2), q2 = fmul2(pair(xf, e), c2);
-                            o[e] = fsub(p2.x, q2.x);
-                            o[e + 1] = fsub(p2.y, q2.y);
-                            const float2 xr = fmul2(pair(xf, e), r2);
-                            const float2 t2 = fmul2(pair(gf, e), xr);
-                            acc[e] = fadd(acc[e], t2.x);
-                            acc[e + 1] = fadd(acc[e + 1], t2.y);
-                            const float2 dz2 = fmul2(pair(gd, e), fmul2(xr, pair(we, e)));
-                            dzv[e] = dz2.x;
-                            dzv[e + 1] = dz2.y;
-                        }
-                    } else {
-#pragma unroll
-                        for (int e = 0; e < 8; ++e) {
-                            o[e] = fsub(fmul(gw[e], r), fmul(xf[e], coef));
-                            const float xr = fmul(xf[e], r);
-                            acc[e] = fadd(acc[e], fmul(gf[e], xr));
-                            dzv[e] = fmul(gd[e], fmul(xr, we[e]));
-                        }
+                    for (int e = 0; e < 8; ++e) {
+                        o[e] = fsub(fmul(gw[e], r), fmul(xf[e], coef));
+                        const float xr = fmul(xf[e], r);
+                        acc[e] = fadd(acc[e], fmul(gf[e], xr));
+                        dzv[e] = fmul(gd[e], fmul(xr, we[e]));
                     }
                     st_global_cs(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
                     st_global_cs(a.dz + row * a.lddz + 8 * l, pack_act<F16>(dzv));
@@ -545,15 +489,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                 for (int q = 1; q < P; ++q) t = fadd(t, cb[q * D + col]);
                 st_global_f1_hint(a.partials + chunk * D + col, t, keep);
             }
-            if (RMSN_NARROW_COMB_BUFS == 1) {
-                // one buffer: everyone has read it before anyone writes the next chunk's totals
-                if (!named_bar_and(kNarrowConsumerBarrier, kNarrowThreads, 1)) {
-                    if (tid == 0) atomicOr(&g_narrow_error, kErrWaitTimeout);
-                    return;
-                }
-            } else {
-                cbuf ^= 1;
-            }
+            cbuf ^= 1;
         }
     }
     pdl_release();
@@ -617,7 +553,7 @@ cudaError_t nbwd_t(const BwdArgs& a, cudaStream_t st) {
     if (e == cudaSuccess) e = encode_vec_1d(&m.rstd, a.rstd, a.T, RS);
     if (e != cudaSuccess) return e;
     const size_t stage = static_cast<size_t>(NIN) * RS * a.D * 2 + RS * 4;
-    const size_t fixed = static_cast<size_t>(RMSN_NARROW_COMB_BUFS) * P * a.D * 4;
+    const size_t fixed = static_cast<size_t>(2) * P * a.D * 4;
     const int S = narrow_stages(RMSN_NARROW_BWD_SMEM, stage, fixed);
     const size_t smem = S * (stage + 16) + fixed;
     if (smem > static_cast<size_t>(kMaxSmem)) return cudaErrorInvalidConfiguration;

@@ -89,9 +89,6 @@
 #ifndef RMSN_BWD_HOLD_WIDE
 #define RMSN_BWD_HOLD_WIDE 1  // VPT 4 at 512 threads: re-read staged operands after the reduction
 #endif
-#ifndef RMSN_BWD_GATE_KEEP
-#define RMSN_BWD_GATE_KEEP 0
-#endif
 #ifndef RMSN_BWD_DIET_224
 #define RMSN_BWD_DIET_224 1  // VPT 4 at 224 threads, modes streaming 3-4 operands: HOLD and WL1 as well
 #endif
@@ -499,12 +496,12 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // stage is released at the end of the iteration); WL1 reads the weights
     // from L1 where they are used instead of keeping them in registers.
     // Measured at D=16384: 783 -> 667 us per 32768 rows; at 256 threads
-    // (D <= 8192) both cost more than they save.
+    // (D <= 8192) both cost more than they save. The 224-thread kernel
+    // (4096 < D <= 7168, 128 registers) takes both in the modes that stream
+    // three or four operands, where it spilled 248-344 bytes a thread without
+    // them (32768 x 7168 backward with pass 2: gated 661 -> 542 us, fused add
+    // 521 -> 495, residual 339 -> 322; the plain mode does not spill there).
     constexpr bool V4_224_DIET = VPT == 4 && MAXT == 224 && M != kPlain && RMSN_BWD_DIET_224;
-    // GK (gated): the gate and its derivative are evaluated once, before the
-    // row reduction, and g q(z), g q'(z) are kept across it, instead of
-    // evaluating the gate again after it.
-    constexpr bool GK = M == kGated && RMSN_BWD_GATE_KEEP;
     constexpr bool HOLD = (VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE) || V4_224_DIET;
     constexpr bool WL1 = (VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE) || V4_224_DIET;
     // Element pairs through the packed fp32 instructions (same bits as the
@@ -618,7 +615,6 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         float gx[R][VPT][8];  // g*x       (gated: g*q(z)*x)
         float tz[R][VPT][8];  // residual: g_res; gated: z, then q(z); fused add: res
         float g0[R][VPT][8];  // gated: g q'(z)
-        float gq[R][VPT][8];  // gated with GK: g q(z), kept across the row reduction
         float rr[R];
         float sp[R];          // this thread's part of s = sum g x w_eff (gated: g q x w_eff)
         uint4 gv[R][VPT], xv[R][VPT], tv[R][VPT], fv[R][VPT];  // fv: fused add's g_res
@@ -670,15 +666,14 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         if (M == kGated) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                if (RMSN_BWD_LEAN && !GK) {
+                                if (RMSN_BWD_LEAN) {
                                     gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));  // g*q(z)
-                                } else {  // kept: g*q'(z) in g0, q(z) in tz, g*q(z) in gq
+                                } else {  // kept: g*q'(z) in g0, q(z) in tz
                                     float q, dq;
                                     gate_eval<SIG>(tz[r][j][e], q, dq);
                                     g0[r][j][e] = fmul(gf[e], dq);
                                     tz[r][j][e] = q;
                                     gf[e] = fmul(gf[e], q);
-                                    gq[r][j][e] = gf[e];
                                 }
                             }
                         }
@@ -738,19 +733,12 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
                         }
                         if (RMSN_BWD_LEAN) {
-                            // Recompute the phase-1 products from the packed row (same bits);
-                            // GK: from the kept g*q(z) and the packed x.
+                            // Recompute the phase-1 products from the packed row (same bits).
                             float gf[8];
-                            if (GK) {
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) gf[e] = gq[r][j][e];
-                                norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
-                            } else {
-                                unpack_act<F16>(gv[r][j], gf);
-                                norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
-                                if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
-                            }
-                            if (M == kGated && !GK) {
+                            unpack_act<F16>(gv[r][j], gf);
+                            norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
+                            if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
+                            if (M == kGated) {
                                 // The gate and its derivative, once: g*q'(z) in g0, q(z) in tz.
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
