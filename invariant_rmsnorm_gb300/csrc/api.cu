@@ -8,6 +8,8 @@
 #include <mutex>
 #include <tuple>
 
+#include <cudaTypedefs.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -128,7 +130,7 @@ int64_t num_chunks(int64_t T, int D) {
 namespace {
 std::mutex g_mu;
 std::map<int, int> g_sms;
-std::map<std::tuple<int, const void*>, int> g_smem_set;
+std::map<std::tuple<int, unsigned long long, const void*>, int> g_smem_set;
 std::map<std::tuple<int, const void*, int, int>, int> g_occ;
 
 int current_device() {
@@ -137,6 +139,31 @@ int current_device() {
     return d;
 }
 }  // namespace
+
+// The current context's unique id, through the driver entry points (the
+// library does not link libcuda); false if there is no current context yet or
+// the driver does not provide them. A context destroyed and created again
+// (cudaDeviceReset) gets a new id, so state kept per context can tell.
+bool current_context_id(unsigned long long* id) {
+    static std::once_flag once;
+    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
+    static PFN_cuCtxGetId_v12000 get_id = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
+    });
+    CUcontext ctx = nullptr;
+    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
+        return false;
+    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
+}
 
 int sm_count() {
     const int dev = current_device();
@@ -152,8 +179,14 @@ int sm_count() {
 cudaError_t ensure_smem_attr(const void* kernel, int bytes) {
     if (bytes <= 48 * 1024) return cudaSuccess;
     const int dev = current_device();
+    // The attribute belongs to the function in the current context: keyed on
+    // the context too, so that it is set again after a device reset (without a
+    // context id it is set on every call).
+    unsigned long long ctx = 0;
+    const bool have_ctx = current_context_id(&ctx);
+    if (!have_ctx) return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     std::lock_guard<std::mutex> lk(g_mu);
-    auto key = std::make_tuple(dev, kernel);
+    auto key = std::make_tuple(dev, ctx, kernel);
     auto it = g_smem_set.find(key);
     if (it != g_smem_set.end() && it->second >= bytes) return cudaSuccess;
     cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
@@ -262,6 +295,14 @@ int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     // (measured 131072 x 8192: 1124 -> 1101 us, with the larger ring the
     // one-CTA-per-SM backward gets).
     if (!c.narrow && a.D / 8 >= RMSN_BWD_NT512_FROM && a.D / 8 <= 4 * RMSN_BWD_NTMAX)
+        wide_shape(a.D / 8, 512, &c.bwd_threads, &c.bwd_vpt);
+    // The modes that stream three or four operands take that shape from
+    // 4096 < D on (two vectors on up to 512 threads, one CTA per SM) instead of
+    // four vectors on 224 threads at two CTAs per SM (32768 x 7168, backward
+    // with pass 2: fused add 499 -> 359 us, residual 323 -> 309, gated
+    // 541 -> 529); the plain backward keeps the 224-thread kernel (232 us either
+    // way). Like every launch shape here it is a function of D and the mode.
+    if (!c.narrow && base_mode(m) != kPlain && a.D / 8 > 512 && a.D / 8 < RMSN_BWD_NT512_FROM)
         wide_shape(a.D / 8, 512, &c.bwd_threads, &c.bwd_vpt);
     // The recompute of y is a compile-time flag of the kernels: the backward
     // without it carries no y code (nor its registers).

@@ -127,6 +127,9 @@ cudaError_t launch_dgamma_reduce(const float* partials, int64_t nchunks, int D, 
 
 // Device properties, cached per device.
 int sm_count();
+// The current context's unique id (false if none is current or the driver
+// cannot say); see api.cu.
+bool current_context_id(unsigned long long* id);
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
 int ctas_per_sm(const void* kernel, int threads, int smem_bytes);
 

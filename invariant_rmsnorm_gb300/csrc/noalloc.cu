@@ -20,8 +20,6 @@
 // it and give wrong weight gradients. Nothing in the array has to start at
 // zero: every partial row the backward reads was written earlier in the same
 // call, so the contents a previous call left behind are never used.
-#include <cudaTypedefs.h>
-
 #include <mutex>
 
 #include "common.cuh"
@@ -39,29 +37,6 @@ struct ScratchEntry {
     void* ptr;
 };
 ScratchEntry g_noalloc[kMaxDevices] = {};
-
-// The current context's unique id, through the driver entry points (the
-// library does not link libcuda). False if the driver does not provide them.
-bool current_context_id(unsigned long long* id) {
-    static std::once_flag once;
-    static PFN_cuCtxGetCurrent_v4000 get_current = nullptr;
-    static PFN_cuCtxGetId_v12000 get_id = nullptr;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 4000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_current = reinterpret_cast<PFN_cuCtxGetCurrent_v4000>(p);
-        p = nullptr;
-        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            get_id = reinterpret_cast<PFN_cuCtxGetId_v12000>(p);
-    });
-    CUcontext ctx = nullptr;
-    if (get_current == nullptr || get_id == nullptr || get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr)
-        return false;
-    return get_id(ctx, id) == CUDA_SUCCESS && *id != 0;
-}
 
 // Device address of the scratch array in the current device's context. In
 // host code the array's name is only a host-side stand-in; the real address

@@ -950,7 +950,7 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
             if (vc) return cudaErrorInvalidValue;
             return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
         case 2:
-            if (big) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 512>(a, c, st);
+            if (big) return vc ? bwd_t<2, MODE, 512, true>(a, c, st) : bwd_t<2, MODE, 512>(a, c, st);
             if (c.bwd_threads <= 128)  // rows of 2 vectors a thread on <= 128 threads
                 return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 128>(a, c, st);
             return vc ? bwd_t<2, MODE, 256, true>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);

@@ -322,7 +322,8 @@ def bwd_row_shape(D: int, mode: str):
     """Consumer threads and 16-byte vectors a thread of the wide backward's row
     reduction, a function of D and the mode: up to 256 threads (512 beyond 1024
     vectors), 1, 2 or 4 vectors each; plain rows of at most 256 vectors on at most
-    128 threads; rows of 897..1024 vectors on 512 threads."""
+    128 threads; rows of 897..1024 vectors on 512 threads, and in every mode but
+    the plain one already rows of 513..896 vectors."""
     NV = D // 8
 
     def shape(ntmax):
@@ -335,7 +336,7 @@ def bwd_row_shape(D: int, mode: str):
     nt, vpt = shape(256)
     if mode == "plain" and NV <= 256:
         nt, vpt = shape(128)
-    if 897 <= NV <= 1024:
+    if 897 <= NV <= 1024 or (mode != "plain" and 513 <= NV <= 896):
         nt, vpt = shape(512)
     return nt, vpt
 
