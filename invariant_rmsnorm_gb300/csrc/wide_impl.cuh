@@ -89,9 +89,6 @@
 #ifndef RMSN_BWD_HOLD_WIDE
 #define RMSN_BWD_HOLD_WIDE 1  // VPT 4 at 512 threads: re-read staged operands after the reduction
 #endif
-#ifndef RMSN_BWD_DIET_224
-#define RMSN_BWD_DIET_224 1  // VPT 4 at 224 threads, modes streaming 3-4 operands: HOLD and WL1 as well
-#endif
 #ifndef RMSN_BWD_WL1_WIDE
 #define RMSN_BWD_WL1_WIDE 1  // VPT 4 at 512 threads: weights from L1 where used
 #endif
@@ -496,14 +493,9 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // stage is released at the end of the iteration); WL1 reads the weights
     // from L1 where they are used instead of keeping them in registers.
     // Measured at D=16384: 783 -> 667 us per 32768 rows; at 256 threads
-    // (D <= 8192) both cost more than they save. The 224-thread kernel
-    // (4096 < D <= 7168, 128 registers) takes both in the modes that stream
-    // three or four operands, where it spilled 248-344 bytes a thread without
-    // them (32768 x 7168 backward with pass 2: gated 661 -> 542 us, fused add
-    // 521 -> 495, residual 339 -> 322; the plain mode does not spill there).
-    constexpr bool V4_224_DIET = VPT == 4 && MAXT == 224 && M != kPlain && RMSN_BWD_DIET_224;
-    constexpr bool HOLD = (VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE) || V4_224_DIET;
-    constexpr bool WL1 = (VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE) || V4_224_DIET;
+    // (D <= 8192) both cost more than they save.
+    constexpr bool HOLD = VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE;
+    constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
     // Element pairs through the packed fp32 instructions (same bits as the
     // scalar loops), where they measured faster: every site of the two-vector
     // kernels on 128 and on 512 threads (131072 x 2048: 282 -> 259 us;
@@ -956,8 +948,12 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
             return vc ? bwd_t<2, MODE, 256, true>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
         case 4:
             if (big) return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 512>(a, c, st);
-            if (RMSN_BWD_V4_224 && c.bwd_threads <= 224)
-                return vc ? bwd_t<4, MODE, 224, true>(a, c, st) : bwd_t<4, MODE, 224>(a, c, st);
+            // Only the plain mode runs four vectors on <= 224 threads (the
+            // others take two vectors on up to 512 threads there, run_bwd).
+            if constexpr (base_mode(MODE) == kPlain) {
+                if (RMSN_BWD_V4_224 && c.bwd_threads <= 224)
+                    return vc ? bwd_t<4, MODE, 224, true>(a, c, st) : bwd_t<4, MODE, 224>(a, c, st);
+            }
             return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 256>(a, c, st);
         default: return cudaErrorInvalidValue;
     }
