@@ -293,9 +293,11 @@ def run_ours(args):
                     fwd_bytes(T, D), 200, stream)
 
     with_cpu = rank == 0 and world == 1 and not args.no_cpu_baseline and not args.main_only
-    cpu = cpu_baseline_sample() if with_cpu else None
+    cpu = cpu_baseline_sample(gpu={"x": wl.x, "w": wl.w, "g": wl.g, "g_res": wl.g_res, "y": y, "x_copy": xc,
+                                   "dx": dx, "rstd": rstd}) if with_cpu else None
     if with_cpu:
         extra["gated_262144x128_cpu_baseline"] = cpu_gated_sample()
+        extra["tiny_16x128_cpu_baseline"] = cpu_tiny_sample()
     peak, peak_kind = peaks()
     bwd_gbs = bwd_pass1_bytes(T, D) / (bwd_ms * 1e-3) / 1e9
     traffic = recorded_traffic()
@@ -595,10 +597,55 @@ def _oracle_step(arrs):
     oracle.residual_bwd(g, x, w, r, gr, False)
 
 
-def cpu_baseline_sample(target_s=10.0):
+def _bf16_ulp(v):
+    """One bf16 ulp at each value (normal range; the subnormal quantum below it)."""
+    import numpy as np
+    _, e = np.frexp(np.abs(v))
+    return np.ldexp(1.0, np.maximum(e - 8, -133))
+
+
+def _ulp_histogram(got, ref, pre=None, scale=None):
+    """Distance of the GPU's bf16 outputs from the oracle's correctly rounded ones:
+    how many are equal, one bf16 ulp away, further but within the cancellation
+    clause (|got - unrounded| <= ulp/2 + 96 * 2^-24 * scale), and beyond."""
+    import numpy as np
+    d = np.abs(got - ref) / _bf16_ulp(ref)
+    h = {"0": int(np.sum(d == 0)), "1": int(np.sum((d > 0) & (d <= 1)))}
+    beyond = d > 1
+    if pre is not None:
+        canc = beyond & (np.abs(got - pre) <= 0.5 * _bf16_ulp(ref) + 96 * 2.0**-24 * scale)
+        h["cancellation"] = int(np.sum(canc))
+        beyond &= ~canc
+    h["beyond"] = int(np.sum(beyond))
+    return h
+
+
+def cpu_baseline_sample(target_s=10.0, gpu=None, rows=2048):
+    """The float64 oracle timed on repeated row samples of the workload. With
+    `gpu` (the benchmark's input and output tensors), the sample is the first
+    `rows` rows of the benchmark's own workload, and the oracle's results on it
+    are also compared with the GPU's outputs for those rows (bf16 ulp
+    histograms of y and dx, rstd's largest relative error, the copy bitwise)."""
+    import numpy as np
+
     import oracle
-    rows = 2048
-    arrs = _oracle_sample(rows)
+    acc = None
+    if gpu is not None:
+        f = lambda t: t[:rows].float().cpu().numpy().astype(np.float64)  # noqa: E731
+        arrs = (f(gpu["x"]), gpu["w"].float().cpu().numpy().astype(np.float64), f(gpu["g"]), f(gpu["g_res"]))
+        x, w, g, gr = arrs
+        y_ref, r_ref, _ = oracle.residual_fwd(x, w, EPS, False)
+        r_gpu = gpu["rstd"][:rows].cpu().numpy().astype(np.float64)
+        dx_ref, _, diag = oracle.residual_bwd(g, x, w, r_gpu, gr, False, diagnostics=True)
+        acc = {"rows": rows, "of": int(gpu["x"].shape[0]),
+               "y_ulp": _ulp_histogram(f(gpu["y"]), y_ref),
+               "dx_ulp": _ulp_histogram(f(gpu["dx"]), dx_ref, diag["dx_pre"], diag["dx_scale"]),
+               "rstd_max_rel_err": float(np.max(np.abs(r_gpu - r_ref) / r_ref)),
+               "x_copy_bitwise": bool(np.array_equal(f(gpu["x_copy"]), x)),
+               "bar": "y, dx within 1 bf16 ulp of the oracle's correctly rounded value (dx: or the "
+                      "cancellation clause); rstd within 1e-5 relative"}
+    else:
+        arrs = _oracle_sample(rows)
     _oracle_step(arrs)
     t0 = time.perf_counter()
     n = 0
@@ -606,9 +653,12 @@ def cpu_baseline_sample(target_s=10.0):
         _oracle_step(arrs)
         n += 1
     dt = time.perf_counter() - t0
-    return {"value": round(n * step_bytes(rows, D_COLS) / dt / 1e9, 4), "unit": "GB/s",
-            "cores": oracle.num_threads(), "kind": "oracle",
-            "sample": f"{n} repetitions of {rows} rows x {D_COLS} (residual fwd+bwd, float64 C oracle), {dt:.1f} s"}
+    out = {"value": round(n * step_bytes(rows, D_COLS) / dt / 1e9, 4), "unit": "GB/s",
+           "cores": oracle.num_threads(), "kind": "oracle",
+           "sample": f"{n} repetitions of {rows} rows x {D_COLS} (residual fwd+bwd, float64 C oracle), {dt:.1f} s"}
+    if acc is not None:
+        out["accuracy_of_the_gpu_outputs_on_the_sample"] = acc
+    return out
 
 
 def cpu_gated_sample(target_s=5.0, rows=8192):
@@ -636,6 +686,32 @@ def cpu_gated_sample(target_s=5.0, rows=8192):
     return {"value": round(n * rows * (16 * D + 8) / dt / 1e9, 4), "unit": "GB/s",
             "rows_per_s": round(n * rows / dt), "cores": oracle.num_threads(), "kind": "oracle",
             "sample": f"{n} repetitions of {rows} rows x {D} (gated fwd+bwd, float64 C oracle), {dt:.1f} s"}
+
+
+def cpu_tiny_sample(reps=200):
+    """The oracle on the tiny plain fwd+bwd (T=16, D=128, zero-centred gamma
+    off and on): wall clock per call, best of 3 runs of `reps` calls."""
+    import numpy as np
+
+    import oracle
+    from invariant_rmsnorm_gb300 import synth
+    res = {}
+    for zc in (False, True):
+        wl = synth.tiny_plain("cpu", seed=0, zero_centered_gamma=zc)
+        f = lambda t: t.float().numpy().astype(np.float64)  # noqa: E731
+        x, w, g = f(wl.x), f(wl.w), f(wl.g)
+        best = float("inf")
+        for _ in range(3):
+            t0 = time.perf_counter()
+            for _ in range(reps):
+                _, r = oracle.rmsnorm_fwd(x, w, EPS, zc)
+                oracle.rmsnorm_bwd(g, x, w, r, zc)
+            best = min(best, (time.perf_counter() - t0) / reps)
+        res[f"zero_centered_gamma={zc}"] = {"us_per_step": round(best * 1e6, 2),
+                                             "rows_per_s": round(wl.T / best)}
+    res.update({"cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"best of 3 runs of {reps} fwd+bwd calls on the whole 16 x 128 problem"})
+    return res
 
 
 def run_reference(args):

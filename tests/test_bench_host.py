@@ -36,3 +36,22 @@ def test_algorithmic_bytes_count_each_tensor_once():
     assert bench.fwd_bytes(T, D) == T * fwd
     assert bench.bwd_pass1_bytes(T, D) == T * bwd
     assert bench.step_bytes(T, D) == T * (fwd + bwd) == 1_879_310_336
+
+
+def test_ulp_histogram_of_the_bench_accuracy_sample():
+    """The bench's accuracy sample counts each output's distance from the
+    oracle's correctly rounded value in bf16 ulps: 0, 1, further but inside the
+    cancellation clause, beyond."""
+    import numpy as np
+    ref = np.array([1.0, 1.0, -3.0, 0.0078125, 1.0, 1.0])
+    ulp = bench._bf16_ulp(ref)
+    assert ulp[0] == 2.0**-7 and ulp[2] == 2.0**-6 and ulp[3] == 2.0**-14
+    got = ref + np.array([0.0, 1.0, -1.0, 0.0, 2.0, 3.0]) * ulp
+    h = bench._ulp_histogram(got, ref)
+    assert h == {"0": 2, "1": 2, "beyond": 2}
+    pre = got.copy()                               # the unrounded value next to what the GPU returned
+    scale = np.array([0.0, 0.0, 0.0, 0.0, 0.0, 1e-12])
+    h = bench._ulp_histogram(got, ref, pre, scale)
+    assert h == {"0": 2, "1": 2, "cancellation": 2, "beyond": 0}
+    h = bench._ulp_histogram(got, ref, ref, scale)  # unrounded = the reference: 2 and 3 ulp are not cancellation
+    assert h == {"0": 2, "1": 2, "cancellation": 0, "beyond": 2}
