@@ -117,6 +117,11 @@ class ClockSampler:
         self.gpu_id = gpu_id
         self.proc = None
         self.lines = []
+        self.first = 0
+
+    def mark(self):
+        """Readings from here on are the ones reported (the GPU under load)."""
+        self.first = len(self.lines)
 
     def start(self):
         try:
@@ -143,7 +148,7 @@ class ClockSampler:
         self._t.join(timeout=2)
         sm, mx, reasons = [], [], set()
         names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
-        for ln in self.lines:
+        for ln in (self.lines[self.first:] or self.lines):
             parts = [p.strip() for p in ln.split(",")]
             if len(parts) < 8:
                 continue
@@ -230,6 +235,19 @@ def run_ours(args):
         if ev:
             ev[3].record(stream)
 
+    # The clock sampler starts before the warm-up, so that its first reading
+    # is taken while the GPU is idle and the warm-up then brings the clocks up
+    # to their working level before the timed steps (a pause right before them
+    # would let the GPU clock down and slow the first timed steps).
+    gpu_id = "0"
+    try:
+        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        gpu_id = str(dev.index or 0)
+    sampler = ClockSampler(gpu_id)
+    sampler.start()
+    time.sleep(0.25)  # let the sampler take its first reading
+    sampler.mark()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
@@ -241,16 +259,8 @@ def run_ours(args):
     sampled = list(range(0, args.steps, 16))
     evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for k in sampled}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    gpu_id = "0"
-    try:
-        gpu_id = "GPU-" + str(torch.cuda.get_device_properties(dev).uuid)
-    except Exception:
-        gpu_id = str(dev.index or 0)
-    sampler = ClockSampler(gpu_id)
     barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.25)  # let the sampler take its first reading
     start.record(stream)
     for k in range(args.steps):
         step(evs.get(k))
@@ -371,17 +381,18 @@ def run_gated(args):
         if ev:
             ev[3].record(stream)
 
+    sampler = ClockSampler(str(dev.index or 0))
+    sampler.start()
+    time.sleep(0.25)  # first reading while idle; the warm-up then brings the clocks up
+    sampler.mark()
     for _ in range(args.warmup):
         step()
     torch.cuda.synchronize()
     sampled = list(range(0, args.steps, 16))
     evs = {k: [torch.cuda.Event(enable_timing=True) for _ in range(4)] for k in sampled}
     start, stop = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    sampler = ClockSampler(str(dev.index or 0))
     barrier()
     torch.cuda.synchronize()
-    sampler.start()
-    time.sleep(0.25)
     start.record(stream)
     for k in range(args.steps):
         step(evs.get(k))
@@ -512,6 +523,28 @@ def side_measurements(rn, synth, dev, stream, reps=50):
         rn.rmsnorm_bwd(wl.g, wl.x, wl.w, r, dx, dg, ws, False, stream=stream)
     rec("plain_fwd_bwd_gbs", plain, T, 10 * D + 8)
     del wl, y, dx, r, dg, ws
+    # the tiny problem (T=16, D=128, zero-centred gamma off and on): launch-bound, reported per step
+    for zc in (False, True):
+        wl = synth.tiny_plain(dev, seed=0, zero_centered_gamma=zc)
+        y, dx = torch.empty_like(wl.x), torch.empty_like(wl.x)
+        r, dg, ws = buffers(wl.T, wl.D)
+
+        def tiny():
+            rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, zc, stream=stream)
+            rn.rmsnorm_bwd(wl.g, wl.x, wl.w, r, dx, dg, ws, zc, stream=stream)
+        rec(f"tiny_16x128_zc{int(zc)}_fwd_bwd", tiny, wl.T, 10 * wl.D + 8)
+        del wl, y, dx, r, dg, ws
+    # the large sweep: plain fwd+bwd with 0.1 % outlier entries, 10*D + 8 bytes per row
+    for T, D in ((131072, 2048), (131072, 4096), (131072, 7168), (131072, 8192), (262144, 4096)):
+        wl = synth.large(dev, seed=1, T=T, D=D)
+        y, dx = torch.empty_like(wl.x), torch.empty_like(wl.x)
+        r, dg, ws = buffers(T, D)
+
+        def large():
+            rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, False, stream=stream)
+            rn.rmsnorm_bwd(wl.g, wl.x, wl.w, r, dx, dg, ws, False, stream=stream)
+        rec(f"large_{T}x{D}_fwd_bwd_gbs", large, T, 10 * D + 8)
+        del wl, y, dx, r, dg, ws
     # the residual step at the pages' two larger row counts (D = 4096): 14*D + 8 bytes per row
     for T in (131072, 262144):
         wl = synth.residual(dev, seed=11, T=T, D=D)
