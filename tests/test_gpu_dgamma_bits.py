@@ -20,8 +20,8 @@ lane groups of 1, 2, 8, 16 and 32 lanes a row, whose chunk order is its own
 (lane groups over interleaved rows, then the group totals in order; see
 dgamma_model); on the wide path one vector a thread (264, 1000, and 2048
 outside the plain mode), two vectors on 128 threads (2048 plain), on 256
-(4096) and on 512 (8192), four vectors on 224 (7168) and on 512 threads
-(16384).
+(4096) and on up to 512 (8192; 7168 outside the plain mode), four vectors on
+224 (7168 plain) and on 512 threads (16384).
 """
 from __future__ import annotations
 

@@ -2,8 +2,10 @@
 
 For 2048 < D <= 7168, a T whose 32-row chunks fill fewer than 90 % of their
 rounds of 152 x 2 CTAs gets shorter chunks (17 rows at T = 9729 and 10000, 20
-at T = 12000), taken by the stepping instantiation of the two-vector
-256-thread and four-vector 224-thread backward kernels. The bit-for-bit tests
+at T = 12000), taken by the stepping instantiation of the two-vector backward
+kernels (256 threads up to D = 4096; up to 512 threads beyond, which these
+modes use there; the plain mode's four-vector 224-thread kernel is covered by
+the bit-for-bit tests). The bit-for-bit tests
 cover the plain, residual and fused-add modes there; this file adds the gated
 mode with both gates and the fp16 format, against the float64 oracle with the
 usual tolerances (outputs within one ulp or the cancellation bound, rstd 1e-5
@@ -22,8 +24,8 @@ from tests.gpu_common import DEV, check_bwd, check_fwd, run_bwd, run_fwd
 
 pytestmark = pytest.mark.gpu
 
-# (D, T): the 256-thread two-vector kernel (2056, 4096) and the 224-thread
-# four-vector kernel (7168), each at a T that shortens the chunk
+# (D, T): the 256-thread two-vector kernel (2056, 4096) and the two-vector
+# kernel on up to 512 threads (7168), each at a T that shortens the chunk
 SHAPES = [(2056, 12000), (4096, 10000), (7168, 9729)]
 CASES = [("gated", torch.bfloat16, "silu"), ("gated", torch.bfloat16, "sigmoid"),
          ("gated", torch.float16, "sigmoid"), ("residual", torch.float16, "silu"),
