@@ -17,7 +17,8 @@ namespace rmsn {
 
 // ---------------------------------------------------------------------------
 // Row shape: a pure function of D (this is what makes a row's reduction tree,
-// and therefore its bits, independent of everything but D).
+// and therefore its bits, independent of everything but D; run_bwd adjusts the
+// backward's shape by the variant, which a call fixes).
 // ---------------------------------------------------------------------------
 #ifndef RMSN_FWD_NTMAX
 #define RMSN_FWD_NTMAX 256

@@ -14,11 +14,12 @@
 //     waits for a copy to be issued.
 //   * Consumer thread t owns VPT 16-byte vectors of each row at slots
 //     v = k*NT + t (coalesced, conflict-free shared reads).
-//   * Fixed reduction tree (a function of D only): per-thread ascending sum
-//     over its slots and the 8 elements of each vector, an xor-butterfly over the
-//     warp (offsets 16..1), then the per-warp totals added in warp order. The
-//     R rows of an iteration share one named barrier but each keeps its own
-//     tree, so a row's bits depend on nothing but the row and D: not on T, its
+//   * Fixed reduction tree (a function of D and, in the backward, of the
+//     variant only): per-thread ascending sum over its slots and the 8
+//     elements of each vector, an xor-butterfly over the warp (offsets 16..1),
+//     then the per-warp totals added in warp order. The R rows of an iteration
+//     share one named barrier but each keeps its own tree, so a row's bits
+//     depend on nothing but the row, D and the variant: not on T, its
 //     position, the other rows, the grid or the GPU.
 //   * fp32 arithmetic with every multiply and add rounded separately (no FMA
 //     contraction; in some kernels the products of neighbouring elements go
