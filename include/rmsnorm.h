@@ -20,12 +20,17 @@
  *   dgamma_j = sum_t g_tj x_tj r_t                     fp32
  *
  * Batch invariance: every row is reduced by a fixed tree whose shape depends on
- * D alone, so y[t], rstd[t] and dx[t] are bitwise independent of T, of the row's
- * position, of the other rows and of the GPU's SM count. dgamma is a sum over
+ * D alone (in the backward, on D and the variant called), so y[t], rstd[t] and
+ * dx[t] are bitwise independent of T, of the row's position, of the other rows
+ * and of the GPU's SM count. dgamma is a sum over
  * rows; it is computed with no atomics, in row chunks whose size depends on T
  * and D alone (pass 1), whose partial sums are added in a fixed order (pass 2),
  * so it is bitwise identical from run to run and across GPUs with different
  * SM counts.
+ *
+ * The weight-gradient chunk: every chunk of one call has the same number of
+ * rows (only the last may be shorter), a function of T and D only ("fixed-size
+ * row chunks" read as fixed for a given problem shape).
  *
  * Common conventions for every entry point:
  *   - Activations (x, z, g, g_res, y, dx, dz, x_copy) are bf16 (fp16 as an
@@ -153,6 +158,8 @@ int rmsnorm_gated_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64
  * convention divergence ([ZC-norm]: the two upstreams round the gated norm
  * differently; they agree bitwise with fp32 inputs). Forward only:
  *   n = bf16((x * r)),  t = bf16(bf16(w_eff) * n),  y = bf16(t * silu(z)).
+ * The pages give no cast points, only that this convention's weight multiply is
+ * not an fp32 one: these are the library's reading of them.
  * Arguments as rmsnorm_gated_fwd. */
 int rmsnorm_gated_hf_fwd(const rmsn_bf16* x, int64_t ldx, const rmsn_bf16* z, int64_t ldz,
                          const float* w, rmsn_bf16* y, int64_t ldy, float* rstd,
