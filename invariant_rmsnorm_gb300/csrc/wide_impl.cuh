@@ -87,6 +87,9 @@
 #ifndef RMSN_BWD_V4_224
 #define RMSN_BWD_V4_224 1  // VPT 4 rows of at most 224 threads: a 224-thread kernel, 2 CTAs per SM
 #endif
+#ifndef RMSN_BWD_SGS
+#define RMSN_BWD_SGS 1  // gated (silu) backward at one or two vectors a thread: sigmoid(z) parked in shared memory
+#endif
 #ifndef RMSN_BWD_HOLD_WIDE
 #define RMSN_BWD_HOLD_WIDE 1  // VPT 4 at 512 threads: re-read staged operands after the reduction
 #endif
@@ -496,6 +499,15 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // Measured at D=16384: 783 -> 667 us per 32768 rows; at 256 threads
     // (D <= 8192) both cost more than they save.
     constexpr bool HOLD = VPT == 4 && MAXT > 256 && RMSN_BWD_HOLD_WIDE;
+    // SGS (silu gate, one or two vectors a thread): sigmoid(z), computed once
+    // before the row reduction, is parked in this thread's own shared-memory
+    // slots and read back after it, so the gate's exponential and reciprocal
+    // run once per element instead of twice (q = z sigmoid(z) again has the
+    // same bits; q' = sigmoid(z) + q (1 - sigmoid(z)), accurate to a few fp32
+    // ulps of its terms). 32768 rows, backward with pass 2: D=2048 139 -> 124
+    // us, 4096 257 -> 239, 7168 529 -> 479, 8192 552 -> 509. Parking q and q'
+    // for both gates instead needed more registers and gained less.
+    constexpr bool SGS = M == kGated && !SIG && VPT <= 2 && RMSN_BWD_LEAN && RMSN_BWD_SGS;
     constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
     // Element pairs through the packed fp32 instructions (same bits as the
     // scalar loops), where they measured faster: every site of the two-vector
@@ -526,6 +538,9 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     uint64_t* empty = full + S;
     float* rs = reinterpret_cast<float*>(empty + S);  // [S][R]
     float* red = rs + S * R;                          // [2][R][32]
+    // SGS: [R][VPT][2][nt][4] sigmoid(z), read and written as float4: 16-byte
+    // aligned (red ends on a 4-byte boundary only, e.g. with R = 2 and an odd S).
+    float* sgs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(red + 2 * R * 32) + 15) & ~uintptr_t(15));
 
     // This CTA's chunks: cta, cta+G, ...; only the globally last chunk can be
     // short, and if this CTA owns it, it is its last one.
@@ -659,7 +674,10 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                         if (M == kGated) {
 #pragma unroll
                             for (int e = 0; e < 8; ++e) {
-                                if (RMSN_BWD_LEAN) {
+                                if (SGS) {
+                                    g0[r][j][e] = sigmoidf_rn(tz[r][j][e]);  // sigmoid(z), parked below
+                                    gf[e] = fmul(gf[e], fmul(tz[r][j][e], g0[r][j][e]));  // g*q(z)
+                                } else if (RMSN_BWD_LEAN) {
                                     gf[e] = fmul(gf[e], gate_value<SIG>(tz[r][j][e]));  // g*q(z)
                                 } else {  // kept: g*q'(z) in g0, q(z) in tz
                                     float q, dq;
@@ -668,6 +686,11 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                     tz[r][j][e] = q;
                                     gf[e] = fmul(gf[e], q);
                                 }
+                            }
+                            if constexpr (SGS) {
+                                float4* slot = reinterpret_cast<float4*>(sgs) + ((r * VPT + j) * 2) * nt + tid;
+                                slot[0] = make_float4(g0[r][j][0], g0[r][j][1], g0[r][j][2], g0[r][j][3]);
+                                slot[nt] = make_float4(g0[r][j][4], g0[r][j][5], g0[r][j][6], g0[r][j][7]);
                             }
                         }
                         if constexpr (X2P1) {
@@ -731,7 +754,21 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                             unpack_act<F16>(gv[r][j], gf);
                             norm_input<MODE>(xv[r][j], tv[r][j], xs[r][j]);
                             if (M == kResidual || M == kGated) unpack_act<F16>(tv[r][j], tz[r][j]);
-                            if (M == kGated) {
+                            if constexpr (SGS) {
+                                // sigmoid(z) from the slots; q = z sigmoid(z) (the same bits as
+                                // before the reduction), q' = sigmoid(z) + q (1 - sigmoid(z)).
+                                const float4* slot = reinterpret_cast<const float4*>(sgs) + ((r * VPT + j) * 2) * nt + tid;
+                                const float4 lo = slot[0], hi = slot[nt];
+                                const float sg[8] = {lo.x, lo.y, lo.z, lo.w, hi.x, hi.y, hi.z, hi.w};
+#pragma unroll
+                                for (int e = 0; e < 8; ++e) {
+                                    const float q = fmul(tz[r][j][e], sg[e]);
+                                    const float dq = fadd(sg[e], fmul(q, fsub(1.0f, sg[e])));
+                                    g0[r][j][e] = fmul(gf[e], dq);
+                                    tz[r][j][e] = q;
+                                    gf[e] = fmul(gf[e], q);
+                                }
+                            } else if (M == kGated) {
                                 // The gate and its derivative, once: g*q'(z) in g0, q(z) in tz.
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
@@ -905,8 +942,10 @@ template <int VPT, int MODE, int MAXT, bool VC = false>
 cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     constexpr int NIN = bwd_inputs(MODE);
     constexpr int R = bwd_rows<VPT, MAXT>();
+    constexpr bool SGS = base_mode(MODE) == kGated && !is_sigmoid_gate(MODE) && VPT <= 2 && RMSN_BWD_LEAN &&
+                         RMSN_BWD_SGS;
     const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
-    const size_t fixed = 2 * R * 32 * 4;
+    const size_t fixed = 2 * R * 32 * 4 + (SGS ? 16 + static_cast<size_t>(R) * VPT * 8 * c.bwd_threads * 4 : 0);
     const int S = stages_for(MAXT > 256 ? RMSN_WIDE_BWD_SMEM_512 : RMSN_WIDE_BWD_SMEM, stage, 16 + 4 * R, fixed);
     const size_t smem = S * (stage + 16 + 4 * R) + fixed;
     if (smem > static_cast<size_t>(kMaxSmemPerCta)) return cudaErrorInvalidConfiguration;
