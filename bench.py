@@ -593,6 +593,23 @@ def side_measurements(rn, synth, dev, stream, reps=50):
         T, 6 * D + 4)
     rec(f"plain_fwd_{T}x{D}_gbs", lambda: rn.rmsnorm_fwd(wl.x, wl.w, y, r, EPS, False, stream=stream), T, 4 * D + 4)
     del wl, y, dx, r, dg, ws
+    # the widest rows in the modes that stream three or four operands a row (CTA
+    # pairs): residual (8*D + 4 bytes per row), gated and fused add (10*D + 4)
+    x = synth.normal_bf16((T, D), 13, dev)
+    z = synth.normal_bf16((T, D), 14, dev)
+    gg = synth.normal_bf16((T, D), 15, dev)
+    gr = synth.normal_bf16((T, D), 16, dev)
+    w = synth.gamma_f32(D, 17, dev)
+    y, dx, dz = torch.empty_like(x), torch.empty_like(x), torch.empty_like(x)
+    r, dg, ws = buffers(T, D)
+    rn.rmsnorm_fwd(x, w, y, r, EPS, False, stream=stream)
+    rec(f"residual_bwd_{T}x{D}_gbs",
+        lambda: rn.rmsnorm_residual_bwd(gg, x, w, r, gr, dx, dg, ws, False, stream=stream), T, 8 * D + 4)
+    rec(f"gated_bwd_{T}x{D}_gbs",
+        lambda: rn.rmsnorm_gated_bwd(gg, x, z, w, r, dx, dz, dg, ws, True, stream=stream), T, 10 * D + 4)
+    rec(f"fused_add_bwd_{T}x{D}_gbs",
+        lambda: rn.rmsnorm_fused_add_bwd(gg, x, z, w, r, gr, dx, dg, ws, False, stream=stream), T, 10 * D + 4)
+    del x, z, gg, gr, w, y, dx, dz, r, dg, ws
     return res
 
 

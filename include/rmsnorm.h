@@ -22,7 +22,10 @@
  * Batch invariance: every row is reduced by a fixed tree whose shape depends on
  * D alone (in the backward, on D and the variant called), so y[t], rstd[t] and
  * dx[t] are bitwise independent of T, of the row's position, of the other rows
- * and of the GPU's SM count. dgamma is a sum over
+ * and of the GPU's SM count. In the backward of rows wider than 8192 (in the
+ * plain variant, of 8193..9216 only) the tree has one more level: the row's two
+ * column halves are reduced by the two CTAs of a thread-block cluster and their
+ * sums added, first half first. dgamma is a sum over
  * rows; it is computed with no atomics, in row chunks whose size depends on T
  * and D alone (pass 1), whose partial sums are added in a fixed order (pass 2),
  * so it is bitwise identical from run to run and across GPUs with different

@@ -23,6 +23,9 @@ namespace rmsn {
 #ifndef RMSN_FWD_NTMAX
 #define RMSN_FWD_NTMAX 256
 #endif
+#ifndef RMSN_BWD_PAIR_PLAIN_UPTO
+#define RMSN_BWD_PAIR_PLAIN_UPTO 1152  // plain backward rows of 1025..this many vectors on CTA pairs
+#endif
 #ifndef RMSN_BWD_NTMAX
 #define RMSN_BWD_NTMAX 256
 #endif
@@ -133,6 +136,7 @@ std::mutex g_mu;
 std::map<int, int> g_sms;
 std::map<std::tuple<int, unsigned long long, const void*>, int> g_smem_set;
 std::map<std::tuple<int, const void*, int, int>, int> g_occ;
+std::map<std::tuple<int, const void*, int, int>, int> g_pairs;
 
 int current_device() {
     int d = 0;
@@ -204,6 +208,29 @@ int ctas_per_sm(const void* kernel, int threads, int smem_bytes) {
     int n = 0;
     if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem_bytes) != cudaSuccess) n = 0;
     g_occ[key] = n;
+    return n;
+}
+
+int pair_clusters(const void* kernel, int threads, int smem_bytes) {
+    const int dev = current_device();
+    std::lock_guard<std::mutex> lk(g_mu);
+    auto key = std::make_tuple(dev, kernel, threads, smem_bytes);
+    auto it = g_pairs.find(key);
+    if (it != g_pairs.end()) return it->second;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(2);
+    cfg.blockDim = dim3(threads);
+    cfg.dynamicSmemBytes = smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kernel, &cfg) != cudaSuccess) n = 0;
+    g_pairs[key] = n;
     return n;
 }
 
@@ -305,6 +332,18 @@ int run_bwd(int m, BwdArgs a, float* dgamma, cudaStream_t s) {
     // way). Like every launch shape here it is a function of D and the mode.
     if (!c.narrow && base_mode(m) != kPlain && a.D / 8 > 512 && a.D / 8 < RMSN_BWD_NT512_FROM)
         wide_shape(a.D / 8, 512, &c.bwd_threads, &c.bwd_vpt);
+    // Rows of more than 1024 vectors (D > 8192): each row split between the two
+    // CTAs of a cluster, ceil(NV/2) vectors on up to 512 threads, two vectors
+    // each, in place of four vectors a thread on 512 threads (which spilled in
+    // the modes that stream three or four operands). 32768 rows, backward with
+    // pass 2, D=16384: residual 944 -> 738 us, gated 1926 -> 1118, fused add
+    // 1570 -> 858. The plain mode takes pairs only up to 1152 vectors (D=9216:
+    // 412 -> 393 us): wider, its one CTA pair per two SMs measured slower than
+    // the four-vector kernel (D=16384: 622 against 665 us).
+    if (!c.narrow && a.D / 8 > 4 * RMSN_BWD_NTMAX && (base_mode(m) != kPlain || a.D / 8 <= RMSN_BWD_PAIR_PLAIN_UPTO)) {
+        wide_shape((a.D / 8 + 1) / 2, 512, &c.bwd_threads, &c.bwd_vpt);
+        c.bwd_pair = true;
+    }
     // The recompute of y is a compile-time flag of the kernels: the backward
     // without it carries no y code (nor its registers).
     const int mr = a.y != nullptr ? (m | kFlagRecompute) : m;

@@ -85,6 +85,29 @@ cudaError_t launch_kernel(void (*kern)(Params...), unsigned grid, unsigned block
     return e != cudaSuccess ? e : cudaGetLastError();
 }
 
+// The same launch for a grid of CTA pairs (thread-block clusters of two
+// consecutive CTAs); `grid` is even.
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel_pair(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem,
+                               cudaStream_t st, Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(block);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = RMSN_PDL ? 2 : 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // ---------------------------------------------------------------------------
 // PTX wrappers
 // ---------------------------------------------------------------------------
@@ -137,6 +160,46 @@ __device__ __forceinline__ int named_bar_and(int id, int nthreads, int pred) {
     return res;
 }
 
+// Thread-block clusters: this CTA's rank in its cluster, the cluster's index
+// along x and the number of clusters along x.
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_id_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%clusterid.x;" : "=r"(r));
+    return r;
+}
+__device__ __forceinline__ uint32_t cluster_count_x() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%nclusterid.x;" : "=r"(r));
+    return r;
+}
+
+// The shared::cluster address of the location `p` (in this CTA's shared
+// memory) has in the CTA of rank `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Store 4 bytes into another CTA's shared memory (both addresses from
+// cluster_map, in that CTA); its mbarrier counts them as transaction bytes.
+__device__ __forceinline__ void st_async_f32(uint32_t remote_dst, float v, uint32_t remote_bar) {
+    asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];"
+                 ::"r"(remote_dst), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
+}
+
+// Every thread of every CTA of the cluster (release, then acquire); used once,
+// after the shared-memory barriers are initialised and before any CTA touches
+// another's shared memory.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
 // Bounded wait for the phase with parity `parity` to complete. Returns false if
 // `limit_ns` (the kernels use kWaitTimeoutNs) of global time elapsed without
 // completion.
@@ -156,6 +219,27 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
             const unsigned long long now = global_timer_ns();
             if (it == 0) t0 = now;
             else if (now - t0 > limit_ns) return false;
+        }
+    }
+}
+
+// mbar_wait with cluster-scope acquire: for a phase completed by another CTA
+// of the cluster (st_async_f32), whose data is then read here.
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
+    const uint32_t addr = smem_u32(bar);
+    uint32_t done = 0;
+    unsigned long long t0 = 0;
+    for (uint32_t it = 0;; ++it) {
+        asm volatile(
+            "{\n\t.reg .pred p;\n\t"
+            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+            "selp.u32 %0, 1, 0, p;\n\t}"
+            : "=r"(done) : "r"(addr), "r"(parity) : "memory");
+        if (done) return true;
+        if ((it & 255u) == 0u) {
+            const unsigned long long now = global_timer_ns();
+            if (it == 0) t0 = now;
+            else if (now - t0 > kWaitTimeoutNs) return false;
         }
     }
 }

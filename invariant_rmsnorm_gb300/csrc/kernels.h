@@ -84,6 +84,7 @@ struct RowCfg {
     int vpt;             // 16-byte vectors per thread per row (wide forward); 1 (narrow)
     int bwd_threads;     // CTA size (wide backward)
     int bwd_vpt;         // 16-byte vectors per thread per row (wide backward)
+    bool bwd_pair;       // wide backward: each row split between the two CTAs of a cluster
     int group;           // lanes per row (narrow), a power of two <= 32
     int rows_per_stage;  // rows per pipeline stage (narrow); 1 (wide)
     int chunk_rows;      // rows per weight-gradient partial
@@ -132,6 +133,8 @@ int sm_count();
 bool current_context_id(unsigned long long* id);
 cudaError_t ensure_smem_attr(const void* kernel, int bytes);
 int ctas_per_sm(const void* kernel, int threads, int smem_bytes);
+// Clusters of two CTAs of `kernel` that can be resident at once.
+int pair_clusters(const void* kernel, int threads, int smem_bytes);
 
 // Error-word access for each kernel translation unit.
 cudaError_t wide_read_error(unsigned* flags, bool clear);

@@ -475,7 +475,7 @@ __global__ void __launch_bounds__(MAXT + 32) wide_fwd_kernel(const FwdArgs a, co
 // registers (RMSN_BWD_LEAN, the default: the same bits for fewer registers);
 // with RMSN_BWD_LEAN = 0 they are computed once before it and kept.
 // ---------------------------------------------------------------------------
-template <int VPT, int MODE, int MAXT, bool VC = false>
+template <int VPT, int MODE, int MAXT, bool VC = false, bool PAIR = false>
 __global__ void __launch_bounds__(MAXT + 32, bwd_min_blocks<VPT, MAXT, MODE>())
 wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr int M = base_mode(MODE);
@@ -504,8 +504,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     // slots and read back after it, so the gate's exponential and reciprocal
     // run once per element instead of twice (q = z sigmoid(z) again has the
     // same bits; q' = sigmoid(z) + q (1 - sigmoid(z)), accurate to a few fp32
-    // ulps of its terms). 32768 rows, backward with pass 2: D=2048 139 -> 124
-    // us, 4096 257 -> 239, 7168 529 -> 479, 8192 552 -> 509. Parking q and q'
+    // ulps of its terms). 32768 rows, backward with pass 2: D=2048 139 -> 125
+    // us, 4096 257 -> 232, 7168 529 -> 479, 8192 552 -> 488. Parking q and q'
     // for both gates instead needed more registers and gained less.
     constexpr bool SGS = M == kGated && !SIG && VPT <= 2 && RMSN_BWD_LEAN && RMSN_BWD_SGS;
     constexpr bool WL1 = VPT == 4 && MAXT > 256 && RMSN_BWD_WL1_WIDE;
@@ -524,23 +524,40 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr bool X2OUT = (VPT == 2 || V1X2) && RMSN_F32X2;  // dx, the weight-gradient term, dz and y
     extern __shared__ __align__(128) unsigned char smem[];
     const int D = a.D;
-    const int NV = D >> 3;
+    // PAIR (rows of more than 1024 vectors): the two CTAs of a cluster split
+    // every row's columns, rank 0 the first ceil(NV/2) 16-byte vectors and rank
+    // 1 the rest. The pair runs the cluster's chunks; each CTA reduces its half
+    // of the row sum with the tree below, and both add the two halves in rank
+    // order (the same bits in both).
+    const int rank = PAIR ? static_cast<int>(cluster_ctarank()) : 0;
+    const int NVh = ((D >> 3) + 1) >> 1;
+    const int NV = PAIR ? (rank ? (D >> 3) - NVh : NVh) : (D >> 3);  // this CTA's vectors
+    const int64_t cb = PAIR ? static_cast<int64_t>(rank) * NVh * 8 : 0;  // its first column
     const int nt = blockDim.x - 32;  // consumer threads
     const int tid = threadIdx.x;
     const int lane = tid & 31, warp = tid >> 5, nw = nt >> 5;
     const int64_t T = a.T;
-    const int64_t G = gridDim.x;
-    const int64_t cta = blockIdx.x;
+    const int64_t G = PAIR ? static_cast<int64_t>(cluster_count_x()) : static_cast<int64_t>(gridDim.x);
+    const int64_t cta = PAIR ? static_cast<int64_t>(cluster_id_x()) : static_cast<int64_t>(blockIdx.x);
     const int64_t nchunks = (T + C - 1) / C;
-    const uint32_t row_bytes = static_cast<uint32_t>(D) * 2u;
-    const uint32_t stage_bytes = R * NIN * row_bytes;
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + static_cast<size_t>(S) * stage_bytes);
+    // This CTA's bytes of an operand row.
+    const uint32_t row_bytes = PAIR ? static_cast<uint32_t>(NV) * 16u : static_cast<uint32_t>(D) * 2u;
+    // Their stride in a stage: the same in both CTAs of a pair (ceil(NV/2)
+    // vectors), so that the exchange slots after the ring sit at the same
+    // offset in both.
+    const uint32_t row_stride = PAIR ? static_cast<uint32_t>(NVh) * 16u : row_bytes;
+    const uint32_t stage_bytes = R * NIN * row_stride;
+    // SGS: [R][VPT][2][nt][4] sigmoid(z) at the start of shared memory (a
+    // multiple of 1024 bytes, so the ring after it keeps its alignment), read
+    // and written as float4.
+    float* sgs = reinterpret_cast<float*>(smem);
+    unsigned char* ring = smem + (SGS ? static_cast<size_t>(R) * VPT * 2 * nt * 16 : 0);
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + static_cast<size_t>(S) * stage_bytes);
     uint64_t* empty = full + S;
-    float* rs = reinterpret_cast<float*>(empty + S);  // [S][R]
+    uint64_t* xbar = empty + S;                                        // PAIR: [2], the peer's half
+    float* xslot = reinterpret_cast<float*>(xbar + (PAIR ? 2 : 0));    // PAIR: [2]
+    float* rs = xslot + (PAIR ? 2 : 0);               // [S][R]
     float* red = rs + S * R;                          // [2][R][32]
-    // SGS: [R][VPT][2][nt][4] sigmoid(z), read and written as float4: 16-byte
-    // aligned (red ends on a 4-byte boundary only, e.g. with R = 2 and an odd S).
-    float* sgs = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(red + 2 * R * 32) + 15) & ~uintptr_t(15));
 
     // This CTA's chunks: cta, cta+G, ...; only the globally last chunk can be
     // short, and if this CTA owns it, it is its last one.
@@ -560,9 +577,14 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             mbar_init(&full[s], 2);
             mbar_init(&empty[s], nw);
         }
+        if (PAIR) {
+            mbar_init(&xbar[0], 1);
+            mbar_init(&xbar[1], 1);
+        }
         fence_mbar_init();
     }
     __syncthreads();
+    if constexpr (PAIR) cluster_sync_all();  // the peer's barriers exist before any exchange
     pdl_wait();  // first global memory access below
 
     if (warp == nw) {  // producer warp
@@ -576,7 +598,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             int64_t row0 = cta * C;
             int po = 0;
             produce(full, empty, S, n_it, [&](int i, int s) {
-                unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
+                unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
                 const int nvalid = min(n_my - i * R, R);
                 mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(nvalid) * NIN * row_bytes);
                 for (int r = 0; r < nvalid; ++r)
@@ -584,12 +606,13 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                 cp_async_arrive_noinc(&full[s]);
                 for (int r = 0; r < nvalid; ++r) {
                     const int64_t row = VC ? row0 + r : row_of(i * R + r);
-                    unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_bytes;
-                    bulk_g2s(dst, a.g + row * a.ldg, row_bytes, &full[s], pol);
-                    bulk_g2s(dst + row_bytes, a.x + row * a.ldx, row_bytes, &full[s], pol);
+                    unsigned char* dst = st + static_cast<size_t>(r) * NIN * row_stride;
+                    bulk_g2s(dst, a.g + row * a.ldg + cb, row_bytes, &full[s], pol);
+                    bulk_g2s(dst + row_stride, a.x + row * a.ldx + cb, row_bytes, &full[s], pol);
                     if (NIN >= 3)
-                        bulk_g2s(dst + 2 * row_bytes, third + row * ld_third, row_bytes, &full[s], pol);
-                    if (NIN == 4) bulk_g2s(dst + 3 * row_bytes, a.gres + row * a.ldgr, row_bytes, &full[s], pol);
+                        bulk_g2s(dst + 2 * row_stride, third + row * ld_third + cb, row_bytes, &full[s], pol);
+                    if (NIN == 4)
+                        bulk_g2s(dst + 3 * row_stride, a.gres + row * a.ldgr + cb, row_bytes, &full[s], pol);
                 }
                 row0 += R;
                 po += R;
@@ -599,11 +622,16 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                 }
             });
         }
+        if constexpr (PAIR) {  // the pair's closing barrier (see the consumers' end)
+            __syncwarp();
+            cluster_sync_all();
+        }
         return;
     }
 
+    const float* wv = a.w + cb;  // this CTA's weights
     float we[VPT][8];
-    if (!WL1) load_weights<VPT>(a.w, a.zc, NV, nt, tid, we);
+    if (!WL1) load_weights<VPT>(wv, a.zc, NV, nt, tid, we);
     float acc[VPT][8];
 #pragma unroll
     for (int j = 0; j < VPT; ++j)
@@ -613,9 +641,13 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     int s = 0;
     uint32_t ph = 0;
     int kc = 0, ko = 0;  // this iteration's first row: chunk ordinal kc, offset ko within it
+    bool xok = true;     // PAIR: every exchange so far arrived in time
+    // PAIR: the peer's slots and barriers, as this CTA addresses them.
+    const uint32_t peer_xslot = PAIR ? cluster_map(xslot, static_cast<uint32_t>(rank ^ 1)) : 0u;
+    const uint32_t peer_xbar = PAIR ? cluster_map(xbar, static_cast<uint32_t>(rank ^ 1)) : 0u;
     for (int i = 0; i < n_it; ++i) {
-        const bool ok = mbar_wait(&full[s], ph);
-        const unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
+        const bool ok = mbar_wait(&full[s], ph) && xok;
+        const unsigned char* st = ring + static_cast<size_t>(s) * stage_bytes;
         const int nvalid = min(n_my - i * R, R);
 
         float gw[R][VPT][8];  // g*w_eff   (gated: g*q(z)*w_eff)
@@ -631,15 +663,15 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             rr[r] = 0.0f;
             if (r < nvalid) {
                 rr[r] = rs[s * R + r];
-                const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_bytes;
+                const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_stride;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int v = j * nt + tid;
                     if (v < NV) {
                         gv[r][j] = ld_shared_v4(src + 16 * v);
-                        xv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
-                        if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_bytes + 16 * v);
-                        if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
+                        xv[r][j] = ld_shared_v4(src + row_stride + 16 * v);
+                        if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_stride + 16 * v);
+                        if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_stride + 16 * v);
                     }
                 }
             }
@@ -664,7 +696,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                 for (int j = 0; j < VPT; ++j) {
                     if (j * nt + tid < NV) {
                         float gf[8], wj[8];
-                        if (WL1) weights8(a.w, a.zc, j * nt + tid, wj);
+                        if (WL1) weights8(wv, a.zc, j * nt + tid, wj);
                         else
 #pragma unroll
                             for (int e = 0; e < 8; ++e) wj[e] = we[j][e];
@@ -722,31 +754,47 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         float* rb = red + (i & 1) * (R * 32);
         if (!block_partial<R>(sp, rb, lane, warp, nt, ok)) {
             if (tid == 0) consumer_abort(full, S, i, n_it);
+            if (PAIR) break;  // to the closing barrier: the peer may still store into this CTA
             return;
         }
 #pragma unroll
         for (int r = 0; r < R; ++r) {
             if (r < nvalid) {
                 const float r1 = rr[r];
-                const float s_tot = block_total<NWMAX>(rb + r * 32, nw);
+                float s_tot = block_total<NWMAX>(rb + r * 32, nw);
+                if constexpr (PAIR) {
+                    // Exchange the halves (R is 1): thread 0 stores this CTA's half in
+                    // the peer's slot b, whose barrier counts the 4 bytes; every thread
+                    // waits for the peer's half in its own slot and adds the two in
+                    // rank order (the same bits in both CTAs). Slot and barrier b serve
+                    // every other row; a failed wait is voted at the next row.
+                    const int b = i & 1;
+                    if (tid == 0) {
+                        mbar_arrive_expect_tx(&xbar[b], 4u);
+                        st_async_f32(peer_xslot + 4u * b, s_tot, peer_xbar + 8u * b);
+                    }
+                    xok = mbar_wait_cluster(&xbar[b], static_cast<uint32_t>((i >> 1) & 1)) && xok;
+                    const float s_peer = *reinterpret_cast<volatile float*>(&xslot[b]);
+                    s_tot = rank == 0 ? fadd(s_tot, s_peer) : fadd(s_peer, s_tot);
+                }
                 const float coef = fmul(div_by_d(fmul(fmul(r1, r1), r1), D, a.inv_d_pow2), s_tot);
                 const int64_t row = VC ? (cta + static_cast<int64_t>(kc) * G) * C + ko + r : row_of(i * R + r);
-                uint16_t* dxrow = a.dx + row * a.lddx;
+                uint16_t* dxrow = a.dx + row * a.lddx + cb;
 #pragma unroll
                 for (int j = 0; j < VPT; ++j) {
                     const int v = j * nt + tid;
                     if (v < NV) {
                         float wj[8];
-                        if (WL1) weights8(a.w, a.zc, v, wj);
+                        if (WL1) weights8(wv, a.zc, v, wj);
                         else
 #pragma unroll
                             for (int e = 0; e < 8; ++e) wj[e] = we[j][e];
                         if (HOLD) {  // the operands again, from the stage still held
-                            const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_bytes;
+                            const unsigned char* src = st + static_cast<size_t>(r) * NIN * row_stride;
                             gv[r][j] = ld_shared_v4(src + 16 * v);
-                            xv[r][j] = ld_shared_v4(src + row_bytes + 16 * v);
-                            if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_bytes + 16 * v);
-                            if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_bytes + 16 * v);
+                            xv[r][j] = ld_shared_v4(src + row_stride + 16 * v);
+                            if (NIN >= 3) tv[r][j] = ld_shared_v4(src + 2 * row_stride + 16 * v);
+                            if (NIN == 4) fv[r][j] = ld_shared_v4(src + 3 * row_stride + 16 * v);
                         }
                         if (RMSN_BWD_LEAN) {
                             // Recompute the phase-1 products from the packed row (same bits).
@@ -846,8 +894,8 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
                                     yv[e] = fmul(u, tz[r][j][e]);
                                 }
                             }
-                            st_global_cs(a.dz + row * a.lddz + 8 * v, pack_act<F16>(dzv));
-                            if constexpr (RY) st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
+                            st_global_cs(a.dz + row * a.lddz + cb + 8 * v, pack_act<F16>(dzv));
+                            if constexpr (RY) st_global_cs(a.y + row * a.ldy + cb + 8 * v, pack_act<F16>(yv));
                         } else if constexpr (RY) {
                             // The forward output again, from the saved rstd: same operations,
                             // same bits as the forward's y.
@@ -863,7 +911,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xs[r][j][e], r1), wj[e]);
                             }
-                            st_global_cs(a.y + row * a.ldy + 8 * v, pack_act<F16>(yv));
+                            st_global_cs(a.y + row * a.ldy + cb + 8 * v, pack_act<F16>(yv));
                         }
                     }
                 }
@@ -877,7 +925,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
         const int k_last = i * R + nvalid - 1;
         if ((VC ? ko + nvalid == C : (k_last % C0) == C0 - 1) || k_last == n_my - 1) {
             const int64_t chunk = cta + static_cast<int64_t>(VC ? kc : k_last / C0) * G;
-            float* prow = a.partials + chunk * D;
+            float* prow = a.partials + chunk * D + cb;
             // Partials are re-read by pass 2 right away: keep them in L2.
             const uint64_t keep = policy_evict_last();
 #pragma unroll
@@ -896,6 +944,16 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
             ko = 0;
             ++kc;
         }
+    }
+    if constexpr (PAIR) {
+        // The last row's exchange has no next vote: take it here. Then every
+        // thread of both CTAs meets once more, so that neither CTA exits while
+        // the other may still store into its shared memory (after an abort
+        // too: the peer's waits are bounded, so it gets here as well).
+        if (!named_bar_and(kConsumerBarrier, nt, xok ? 1 : 0) && tid == 0) atomicOr(&g_wide_error, kErrWaitTimeout);
+        pdl_release();
+        cluster_sync_all();
+        return;
     }
     pdl_release();
 }
@@ -938,26 +996,41 @@ cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
     return launch_kernel(wide_fwd_kernel<VPT, MODE, MAXT>, static_cast<unsigned>(grid), threads, smem, st, a, S);
 }
 
-template <int VPT, int MODE, int MAXT, bool VC = false>
+template <int VPT, int MODE, int MAXT, bool VC = false, bool PAIR = false>
 cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     constexpr int NIN = bwd_inputs(MODE);
     constexpr int R = bwd_rows<VPT, MAXT>();
+    static_assert(!PAIR || (R == 1 && !VC), "a CTA pair runs one row per iteration in fixed chunks");
     constexpr bool SGS = base_mode(MODE) == kGated && !is_sigmoid_gate(MODE) && VPT <= 2 && RMSN_BWD_LEAN &&
                          RMSN_BWD_SGS;
-    const size_t stage = static_cast<size_t>(R) * NIN * a.D * 2;
-    const size_t fixed = 2 * R * 32 * 4 + (SGS ? 16 + static_cast<size_t>(R) * VPT * 8 * c.bwd_threads * 4 : 0);
+    // A pair's CTA stages its half of the row: ceil(NV/2) vectors at most.
+    const size_t row_bytes = PAIR ? static_cast<size_t>((a.D / 8 + 1) / 2) * 16 : static_cast<size_t>(a.D) * 2;
+    const size_t stage = static_cast<size_t>(R) * NIN * row_bytes;
+    const size_t fixed = 2 * R * 32 * 4 + (SGS ? static_cast<size_t>(R) * VPT * 8 * c.bwd_threads * 4 : 0) +
+                         (PAIR ? 24 : 0);
     const int S = stages_for(MAXT > 256 ? RMSN_WIDE_BWD_SMEM_512 : RMSN_WIDE_BWD_SMEM, stage, 16 + 4 * R, fixed);
     const size_t smem = S * (stage + 16 + 4 * R) + fixed;
     if (smem > static_cast<size_t>(kMaxSmemPerCta)) return cudaErrorInvalidConfiguration;
     const int threads = c.bwd_threads + 32;
-    const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT, VC>);
+    const void* kern = reinterpret_cast<const void*>(wide_bwd_kernel<VPT, MODE, MAXT, VC, PAIR>);
     cudaError_t e = ensure_smem_attr(kern, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const int occ = std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT, MODE>());
-    if (occ < 1) return cudaErrorInvalidConfiguration;
     const int64_t nchunks = (a.T + a.chunk - 1) / a.chunk;
-    const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
-    return launch_kernel(wide_bwd_kernel<VPT, MODE, MAXT, VC>, static_cast<unsigned>(grid), threads, smem, st, a, S);
+    if constexpr (PAIR) {
+        // One pair per chunk, up to the pairs that can be resident at once.
+        const int np = pair_clusters(kern, threads, static_cast<int>(smem));
+        if (np < 1) return cudaErrorInvalidConfiguration;
+        const int64_t pairs = std::min<int64_t>(nchunks, np);
+        return launch_kernel_pair(wide_bwd_kernel<VPT, MODE, MAXT, VC, PAIR>, static_cast<unsigned>(2 * pairs),
+                                  threads, smem, st, a, S);
+    } else {
+        const int occ =
+            std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT, MODE>());
+        if (occ < 1) return cudaErrorInvalidConfiguration;
+        const int64_t grid = std::min<int64_t>(nchunks, static_cast<int64_t>(sm_count()) * occ);
+        return launch_kernel(wide_bwd_kernel<VPT, MODE, MAXT, VC>, static_cast<unsigned>(grid), threads, smem, st,
+                             a, S);
+    }
 }
 
 template <int MODE>
@@ -982,12 +1055,20 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
             if (vc) return cudaErrorInvalidValue;
             return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
         case 2:
+            // Rows of more than 1024 vectors: a CTA pair per row, two vectors a
+            // thread on up to 512 threads in each CTA.
+            if (c.bwd_pair) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 512, false, true>(a, c, st);
             if (big) return vc ? bwd_t<2, MODE, 512, true>(a, c, st) : bwd_t<2, MODE, 512>(a, c, st);
             if (c.bwd_threads <= 128)  // rows of 2 vectors a thread on <= 128 threads
                 return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 128>(a, c, st);
             return vc ? bwd_t<2, MODE, 256, true>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
         case 4:
-            if (big) return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 512>(a, c, st);
+            // Four vectors on 512 threads: the plain mode's rows of more than
+            // 1152 vectors (the other modes run those rows on CTA pairs).
+            if (big) {
+                if constexpr (base_mode(MODE) == kPlain) return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 512>(a, c, st);
+                return cudaErrorInvalidValue;
+            }
             // Only the plain mode runs four vectors on <= 224 threads (the
             // others take two vectors on up to 512 threads there, run_bwd).
             if constexpr (base_mode(MODE) == kPlain) {

@@ -318,27 +318,65 @@ def f32_round_act(v, fmt: str = "bf16") -> np.ndarray:
     return bits.astype(np.uint32).view(np.float32)
 
 
+def _wide_shape(NV: int, ntmax: int):
+    """Threads (a multiple of 32) and vectors a thread for NV vectors on at most
+    ntmax threads (512 beyond 4*ntmax vectors); 1, 2 or 4 vectors each."""
+    if NV > 4 * ntmax:
+        ntmax = 512
+    need = -(-NV // ntmax)
+    vpt = 1 if need <= 1 else (2 if need <= 2 else 4)
+    return -(-(-(-NV // vpt)) // 32) * 32, vpt
+
+
 def bwd_row_shape(D: int, mode: str):
     """Consumer threads and 16-byte vectors a thread of the wide backward's row
-    reduction, a function of D and the mode: up to 256 threads (512 beyond 1024
-    vectors), 1, 2 or 4 vectors each; plain rows of at most 256 vectors on at most
-    128 threads; rows of 897..1024 vectors on 512 threads, and in every mode but
-    the plain one already rows of 513..896 vectors."""
+    reduction, a function of D and the mode: up to 256 threads, 1, 2 or 4
+    vectors each; plain rows of at most 256 vectors on at most 128 threads; rows
+    of 897..1024 vectors on 512 threads, and in every mode but the plain one
+    already rows of 513..896 vectors. Rows of more than 1024 vectors are split
+    between two CTAs (bwd_is_pair): the shape is then each half's, for
+    ceil(NV/2) vectors on up to 512 threads."""
     NV = D // 8
-
-    def shape(ntmax):
-        if NV > 4 * ntmax:
-            ntmax = 512
-        need = -(-NV // ntmax)
-        vpt = 1 if need <= 1 else (2 if need <= 2 else 4)
-        return -(-(-(-NV // vpt)) // 32) * 32, vpt
-
-    nt, vpt = shape(256)
+    if bwd_is_pair(D, mode):
+        return _wide_shape((NV + 1) // 2, 512)
+    nt, vpt = _wide_shape(NV, 256)
     if mode == "plain" and NV <= 256:
-        nt, vpt = shape(128)
+        nt, vpt = _wide_shape(NV, 128)
     if 897 <= NV <= 1024 or (mode != "plain" and 513 <= NV <= 896):
-        nt, vpt = shape(512)
+        nt, vpt = _wide_shape(NV, 512)
     return nt, vpt
+
+
+def bwd_is_pair(D: int, mode: str) -> bool:
+    """Rows of more than 1024 vectors (D > 8192; in the plain mode only up to
+    1152 vectors, D <= 9216): the two CTAs of a cluster take the first
+    ceil(NV/2) vectors and the rest, and add their halves in that order."""
+    NV = D // 8
+    return NV > 1024 and (mode != "plain" or NV <= 1152)
+
+
+def _thread_tree(vec, nt: int, vpt: int):
+    """One CTA's part of the tree over vec [T, NVc, 8]: thread t adds its
+    vectors v = j*nt + t (j ascending, the 8 elements of each in order) from 0,
+    an xor butterfly over each warp (offsets 16..1), the warp totals in order."""
+    T, NVc = vec.shape[0], vec.shape[1]
+    th = np.zeros((T, nt), np.float32)
+    for j in range(vpt):
+        for t0 in range(nt):
+            v = j * nt + t0
+            if v < NVc:
+                for e in range(8):
+                    th[:, t0] = th[:, t0] + vec[:, v, e]
+    nw = nt // 32
+    warps = th.reshape(T, nw, 32)
+    o = 16
+    while o > 0:
+        warps = warps + warps[:, :, np.arange(32) ^ o]
+        o //= 2
+    s = warps[:, 0, 0]
+    for i in range(1, nw):
+        s = s + warps[:, i, 0]
+    return s
 
 
 def row_sums_model(terms, D: int, mode: str):
@@ -346,9 +384,11 @@ def row_sums_model(terms, D: int, mode: str):
     consumer thread t adds its elements (vectors v = j*NT + t, j ascending, the 8
     elements of each in order) from 0, an xor butterfly over each warp (offsets
     16..1) gives every lane the warp total, and the warp totals are added in
-    warp order; on the narrow path (D <= 256) each lane of a row's group of
-    G = next_pow2(D/8) lanes adds its 8 elements and a butterfly over the group
-    (offsets G/2..1) gives the total."""
+    warp order; rows of more than 1024 vectors do that over each half (the first
+    ceil(NV/2) vectors, the rest) and add the two totals, first half first; on
+    the narrow path (D <= 256) each lane of a row's group of G = next_pow2(D/8)
+    lanes adds its 8 elements and a butterfly over the group (offsets G/2..1)
+    gives the total."""
     T = terms.shape[0]
     NV = D // 8
     vec = terms.reshape(T, NV, 8)
@@ -365,23 +405,10 @@ def row_sums_model(terms, D: int, mode: str):
             o //= 2
         return lanes[:, 0]
     nt, vpt = bwd_row_shape(D, mode)
-    th = np.zeros((T, nt), np.float32)
-    for j in range(vpt):
-        for t0 in range(nt):
-            v = j * nt + t0
-            if v < NV:
-                for e in range(8):
-                    th[:, t0] = th[:, t0] + vec[:, v, e]
-    nw = nt // 32
-    warps = th.reshape(T, nw, 32)
-    o = 16
-    while o > 0:
-        warps = warps + warps[:, :, np.arange(32) ^ o]
-        o //= 2
-    s = warps[:, 0, 0]
-    for i in range(1, nw):
-        s = s + warps[:, i, 0]
-    return s
+    if bwd_is_pair(D, mode):
+        NVh = (NV + 1) // 2
+        return _thread_tree(vec[:, :NVh], nt, vpt) + _thread_tree(vec[:, NVh:], nt, vpt)
+    return _thread_tree(vec, nt, vpt)
 
 
 def dx_model(g, h, w_eff, r, mode: str, g_res=None, fmt: str = "bf16"):
