@@ -294,6 +294,13 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
     return p;
 }
 
+// L2 policy of ordinary priority (explicitly).
+__device__ __forceinline__ uint64_t policy_evict_normal() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
 // L2 policy for data written now and read back soon (kept resident in L2).
 __device__ __forceinline__ uint64_t policy_evict_last() {
     uint64_t p;

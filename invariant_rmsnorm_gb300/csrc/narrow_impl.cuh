@@ -201,7 +201,13 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
         if (lane == 0) {
             prefetch_tensormap(&m.a);
             if (NIN == 2) prefetch_tensormap(&m.b);
-            const uint64_t pol = policy_evict_first();
+            // Ordinary L2 priority for the streamed tiles: at evict_first they
+            // could never displace the lines of higher priority that other
+            // kernels leave in L2 (ordinary stores, evict_last partial rows),
+            // and kept only what those leave free (Qwen3-Next gated step,
+            // 262144 x 128, after such kernels: 95.9 -> 90.5 us; 90.2 us in a
+            // clean L2 either way).
+            const uint64_t pol = policy_evict_normal();
             narrow_produce(full, empty, S, n_it, [&](int i, int s) {
                 unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
                 const int row0 = (cta + i * Gd) * RS;
@@ -349,7 +355,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
             if (NIN >= 3) prefetch_tensormap(&m.c);
             if (NIN == 4) prefetch_tensormap(&m.d);
             prefetch_tensormap(&m.rstd);
-            const uint64_t pol = policy_evict_first();
+            const uint64_t pol = policy_evict_normal();  // as in the forward
             narrow_produce(full, empty, S, n_it, [&](int i, int s) {
                 unsigned char* st = smem + static_cast<size_t>(s) * stage_bytes;
                 const int row0 = block_of(i) * RS;

@@ -118,11 +118,13 @@ template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int fwd_row
     return VPT < 4 ? RMSN_FWD_ROWS
                    : (fwd_inputs(MODE) > 1 ? 1 : (MAXT > 256 ? RMSN_FWD_ROWS_V4 : RMSN_FWD_ROWS_V4_256));
 }
-// Backward CTAs per SM that the register budget must allow, and the cap on
-// resident CTAs: 3 at VPT 1 (72 registers) for the modes that fit there
-// without spilling (not the gated or the fused-add-with-gradient backward), 2
-// at VPT 1 otherwise and at VPT 2 (96), 2 for VPT 4 rows of at most 224
-// threads (128 registers: 4096 < D <= 7168), 1 beyond.
+// Backward CTAs per SM that the register budget must allow: 3 at VPT 1 (72
+// registers) for the modes that fit there without spilling (not the gated or
+// the fused-add backward), 2 at VPT 1 otherwise and at VPT 2 (96), 2 for VPT 4
+// rows of at most 224 threads (128 registers: 4096 < D <= 7168), 1 beyond.
+// The cap on resident CTAs is 3 at VPT 1 in every mode: the gated and
+// fused-add kernels reach it on up to 160 threads at 96 registers (gated,
+// 32768 rows, backward with pass 2: D=512 80.6 -> 62.0 us, 1024 86.7 -> 72.1).
 template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_min_blocks() {
     return MAXT == 128 ? 4 : MAXT == 224 ? 2
            : (MAXT > 256 || VPT > 2) ? 1
@@ -130,9 +132,7 @@ template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_min
                                                                            : RMSN_BWD_MINB;
 }
 template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_ctas_per_sm() {
-    return MAXT == 128 ? 4 : MAXT == 224 ? 2
-           : (VPT == 1 && !is_gated(MODE) && base_mode(MODE) != kFusedAdd) ? RMSN_WIDE_BWD_CTAS_PER_SM_V1
-                                                                           : RMSN_WIDE_BWD_CTAS_PER_SM;
+    return MAXT == 128 ? 4 : MAXT == 224 ? 2 : VPT == 1 ? RMSN_WIDE_BWD_CTAS_PER_SM_V1 : RMSN_WIDE_BWD_CTAS_PER_SM;
 }
 template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_rows() {
     return (VPT == 1 && MAXT <= 256) ? RMSN_BWD_ROWS : 1;

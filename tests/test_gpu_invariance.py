@@ -3,6 +3,10 @@
 1024}, position first / middle / last / shuffled, fresh neighbours, zero padding
 rows, a different row stride — and across repeated runs.
 
+Rows wider than 8192 (12296, 16384, and 9216 in the plain mode) run their
+backward on CTA pairs, whose chunk assignment changes with T; their rows are
+held to the same bar.
+
 Methodology from Expose Batch Invariant Kernels (TransformerEngine issue 2986:
 anchor row at several offsets in batches of different M, output bytes compared
 exactly) and from the zero-centred RMSNorm PR (RL-Kernel pull request 467:
@@ -24,7 +28,7 @@ def _bits(t):
 
 
 @pytest.mark.parametrize("variant,D", [("plain", 4096), ("residual", 4096), ("gated", 128), ("plain", 7168),
-                                       ("plain", 128)])
+                                       ("plain", 128), ("residual", 12296), ("gated", 16384), ("plain", 9216)])
 def test_anchor_row_bitwise_across_batches(variant, D):
     zc = variant == "gated"
     anchor_x = synth.normal_bf16((D,), 100, DEV)
