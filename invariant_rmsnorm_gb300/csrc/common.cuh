@@ -67,45 +67,40 @@ __device__ __forceinline__ void pdl_release() {
 }
 
 // Launch `kern` on `st` (programmatic stream serialization allowed when
-// RMSN_PDL is set). Returns the launch's error.
+// RMSN_PDL is set), in thread-block clusters of `cluster` consecutive CTAs
+// when `cluster` > 1 (`grid` a multiple of it). Returns the launch's error.
 template <typename... Params, typename... Args>
-cudaError_t launch_kernel(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
-                          Args&&... args) {
-    cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(block);
-    cfg.dynamicSmemBytes = smem;
-    cfg.stream = st;
-    cudaLaunchAttribute attr[1];
-    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[0].val.programmaticStreamSerializationAllowed = 1;
-    cfg.attrs = attr;
-    cfg.numAttrs = RMSN_PDL ? 1 : 0;
-    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
-    return e != cudaSuccess ? e : cudaGetLastError();
-}
-
-// The same launch for a grid of CTA pairs (thread-block clusters of two
-// consecutive CTAs); `grid` is even.
-template <typename... Params, typename... Args>
-cudaError_t launch_kernel_pair(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem,
-                               cudaStream_t st, Args&&... args) {
+cudaError_t launch_kernel_clustered(void (*kern)(Params...), unsigned cluster, unsigned grid, unsigned block,
+                                    size_t smem, cudaStream_t st, Args&&... args) {
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
     cfg.blockDim = dim3(block);
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
-    attr[0].id = cudaLaunchAttributeClusterDimension;
-    attr[0].val.clusterDim.x = 2;
-    attr[0].val.clusterDim.y = 1;
-    attr[0].val.clusterDim.z = 1;
-    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-    attr[1].val.programmaticStreamSerializationAllowed = 1;
+    unsigned n = 0;
+    if (RMSN_PDL) {
+        attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[n].val.programmaticStreamSerializationAllowed = 1;
+        ++n;
+    }
+    if (cluster > 1) {
+        attr[n].id = cudaLaunchAttributeClusterDimension;
+        attr[n].val.clusterDim.x = cluster;
+        attr[n].val.clusterDim.y = 1;
+        attr[n].val.clusterDim.z = 1;
+        ++n;
+    }
     cfg.attrs = attr;
-    cfg.numAttrs = RMSN_PDL ? 2 : 1;
+    cfg.numAttrs = n;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+
+template <typename... Params, typename... Args>
+cudaError_t launch_kernel(void (*kern)(Params...), unsigned grid, unsigned block, size_t smem, cudaStream_t st,
+                          Args&&... args) {
+    return launch_kernel_clustered(kern, 1u, grid, block, smem, st, std::forward<Args>(args)...);
 }
 
 // ---------------------------------------------------------------------------
@@ -193,27 +188,36 @@ __device__ __forceinline__ void st_async_f32(uint32_t remote_dst, float v, uint3
                  ::"r"(remote_dst), "r"(__float_as_uint(v)), "r"(remote_bar) : "memory");
 }
 
-// Every thread of every CTA of the cluster (release, then acquire); used once,
-// after the shared-memory barriers are initialised and before any CTA touches
-// another's shared memory.
+// Every thread of every CTA of the cluster (release, then acquire). A CTA pair
+// meets there twice: after the shared-memory barriers are initialised, before
+// either CTA touches the other's shared memory, and at the end, before either
+// exits while the other may still store into it.
 __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
-// Bounded wait for the phase with parity `parity` to complete. Returns false if
-// `limit_ns` (the kernels use kWaitTimeoutNs) of global time elapsed without
-// completion.
-__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
-                                          unsigned long long limit_ns = kWaitTimeoutNs) {
+// Bounded wait for the phase with parity `parity` to complete, with an acquire
+// at CTA scope, or with kCluster at cluster scope (for a phase completed by
+// another CTA of the cluster, st_async_f32, whose data is then read here).
+// Returns false if `limit_ns` of global time elapsed without completion.
+template <bool kCluster>
+__device__ __forceinline__ bool mbar_wait_scoped(uint64_t* bar, uint32_t parity, unsigned long long limit_ns) {
     const uint32_t addr = smem_u32(bar);
     uint32_t done = 0;
     unsigned long long t0 = 0;
     for (uint32_t it = 0;; ++it) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done) : "r"(addr), "r"(parity) : "memory");
+        if constexpr (kCluster)
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(done) : "r"(addr), "r"(parity) : "memory");
+        else
+            asm volatile(
+                "{\n\t.reg .pred p;\n\t"
+                "mbarrier.try_wait.parity.acquire.cta.shared::cta.b64 p, [%1], %2;\n\t"
+                "selp.u32 %0, 1, 0, p;\n\t}"
+                : "=r"(done) : "r"(addr), "r"(parity) : "memory");
         if (done) return true;
         if ((it & 255u) == 0u) {
             const unsigned long long now = global_timer_ns();
@@ -223,25 +227,13 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
     }
 }
 
-// mbar_wait with cluster-scope acquire: for a phase completed by another CTA
-// of the cluster (st_async_f32), whose data is then read here.
+// The kernels' waits: kWaitTimeoutNs unless a test gives another limit.
+__device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity,
+                                          unsigned long long limit_ns = kWaitTimeoutNs) {
+    return mbar_wait_scoped<false>(bar, parity, limit_ns);
+}
 __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity) {
-    const uint32_t addr = smem_u32(bar);
-    uint32_t done = 0;
-    unsigned long long t0 = 0;
-    for (uint32_t it = 0;; ++it) {
-        asm volatile(
-            "{\n\t.reg .pred p;\n\t"
-            "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
-            "selp.u32 %0, 1, 0, p;\n\t}"
-            : "=r"(done) : "r"(addr), "r"(parity) : "memory");
-        if (done) return true;
-        if ((it & 255u) == 0u) {
-            const unsigned long long now = global_timer_ns();
-            if (it == 0) t0 = now;
-            else if (now - t0 > kWaitTimeoutNs) return false;
-        }
-    }
+    return mbar_wait_scoped<true>(bar, parity, kWaitTimeoutNs);
 }
 
 // 1-D bulk copy global -> shared, completion counted on `bar` (bytes).

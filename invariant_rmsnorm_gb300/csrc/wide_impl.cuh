@@ -1021,8 +1021,8 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
         const int np = pair_clusters(kern, threads, static_cast<int>(smem));
         if (np < 1) return cudaErrorInvalidConfiguration;
         const int64_t pairs = std::min<int64_t>(nchunks, np);
-        return launch_kernel_pair(wide_bwd_kernel<VPT, MODE, MAXT, VC, PAIR>, static_cast<unsigned>(2 * pairs),
-                                  threads, smem, st, a, S);
+        return launch_kernel_clustered(wide_bwd_kernel<VPT, MODE, MAXT, VC, PAIR>, 2u,
+                                       static_cast<unsigned>(2 * pairs), threads, smem, st, a, S);
     } else {
         const int occ =
             std::min(ctas_per_sm(kern, threads, static_cast<int>(smem)), bwd_ctas_per_sm<VPT, MAXT, MODE>());
