@@ -74,7 +74,8 @@ def test_zero_centred_differs_and_equals_offset_weight():
 # Shapes: several tiles and a ragged tail, narrow to maximum D
 # ---------------------------------------------------------------------------
 SHAPES = [(D, T) for D in (8, 24, 128, 200, 256, 264, 512, 1032, 2048, 4096, 7168)
-          for T in (1, 70, 333)] + [(8192, 1), (8192, 70), (16384, 1), (16384, 45)]
+          for T in (1, 70, 333)] + [(8192, 1), (8192, 70), (16384, 1), (16384, 45),
+                                    (8200, 33), (9216, 5), (12296, 64)]  # CTA pairs; 12296: unequal halves
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
@@ -84,7 +85,7 @@ def test_shapes(variant, D, T):
 
 
 @pytest.mark.parametrize("variant", VARIANTS)
-@pytest.mark.parametrize("D", [128, 4096])
+@pytest.mark.parametrize("D", [128, 4096, 9216])
 def test_strided_rows(variant, D):
     """Row strides larger than D on every input and output; the gap columns of the
     outputs must be left untouched."""
