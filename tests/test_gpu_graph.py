@@ -3,9 +3,10 @@
 Every kernel is launched with programmatic stream serialization, so in a
 captured graph consecutive kernels are joined by programmatic edges. A graph
 of forward + backward + weight-gradient reduction, replayed, must give the
-eager calls' bits exactly (both row paths, wide and narrow), and replaying it
-on new inputs copied into the captured buffers must match eager calls on
-those inputs.
+eager calls' bits exactly (both row paths, wide and narrow, and the backward
+of rows wider than 8192, launched on two-CTA clusters), and replaying it on
+new inputs copied into the captured buffers must match eager calls on those
+inputs.
 """
 from __future__ import annotations
 
@@ -51,7 +52,8 @@ def _buffers(kind, T, D, seed):
 OUTS = {"residual": ("y", "xc", "rstd", "dx", "dw"), "gated": ("y", "rstd", "dx", "dz", "dw")}
 
 
-@pytest.mark.parametrize("kind,T,D", [("residual", 4096, 4096), ("residual", 1000, 768), ("gated", 20000, 128)])
+@pytest.mark.parametrize("kind,T,D", [("residual", 4096, 4096), ("residual", 1000, 768), ("gated", 20000, 128),
+                                      ("residual", 700, 16384), ("gated", 300, 12296)])  # CTA-pair backwards
 def test_graph_replay_matches_eager(kind, T, D):
     step = _residual_step if kind == "residual" else _gated_step
     b = _buffers(kind, T, D, seed=3)
