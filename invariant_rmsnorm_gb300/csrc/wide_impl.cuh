@@ -84,9 +84,6 @@
 #ifndef RMSN_BWD_MINB_V1
 #define RMSN_BWD_MINB_V1 3  // the same for VPT 1 (3 CTAs of 72 registers)
 #endif
-#ifndef RMSN_BWD_V4_224
-#define RMSN_BWD_V4_224 1  // VPT 4 rows of at most 224 threads: a 224-thread kernel, 2 CTAs per SM
-#endif
 #ifndef RMSN_BWD_SGS
 #define RMSN_BWD_SGS 1  // gated (silu) backward at one or two vectors a thread: sigmoid(z) parked in shared memory
 #endif
@@ -1035,10 +1032,12 @@ cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
 
 template <int MODE>
 cudaError_t fwd_dispatch(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
+    // The shapes row_cfg gives: one and two vectors a thread on up to 256
+    // threads (D <= 4096), four on up to 256 (D <= 8192) or 512 (beyond).
     const bool big = c.threads > 256;
     switch (c.vpt) {
-        case 1: return big ? fwd_t<1, MODE, 512>(a, c, st) : fwd_t<1, MODE, 256>(a, c, st);
-        case 2: return big ? fwd_t<2, MODE, 512>(a, c, st) : fwd_t<2, MODE, 256>(a, c, st);
+        case 1: return big ? cudaErrorInvalidValue : fwd_t<1, MODE, 256>(a, c, st);
+        case 2: return big ? cudaErrorInvalidValue : fwd_t<2, MODE, 256>(a, c, st);
         case 4: return big ? fwd_t<4, MODE, 512>(a, c, st) : fwd_t<4, MODE, 256>(a, c, st);
         default: return cudaErrorInvalidValue;
     }
@@ -1050,32 +1049,29 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     // A chunk other than kWideChunkRows (2048 < D <= 7168 only) runs the
     // stepping instantiation of the two kernels those widths use.
     const bool vc = a.chunk != kWideChunkRows;
+    // Only the shapes run_bwd gives are instantiated; any other returns an error.
     switch (c.bwd_vpt) {
-        case 1:
-            if (vc) return cudaErrorInvalidValue;
-            return big ? bwd_t<1, MODE, 512>(a, c, st) : bwd_t<1, MODE, 256>(a, c, st);
+        case 1:  // D <= 2048: up to 256 threads
+            if (vc || big) return cudaErrorInvalidValue;
+            return bwd_t<1, MODE, 256>(a, c, st);
         case 2:
             // Rows of more than 1024 vectors: a CTA pair per row, two vectors a
             // thread on up to 512 threads in each CTA.
             if (c.bwd_pair) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 512, false, true>(a, c, st);
             if (big) return vc ? bwd_t<2, MODE, 512, true>(a, c, st) : bwd_t<2, MODE, 512>(a, c, st);
-            if (c.bwd_threads <= 128)  // rows of 2 vectors a thread on <= 128 threads
-                return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 128>(a, c, st);
-            return vc ? bwd_t<2, MODE, 256, true>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
-        case 4:
-            // Four vectors on 512 threads: the plain mode's rows of more than
-            // 1152 vectors (the other modes run those rows on CTA pairs).
-            if (big) {
-                if constexpr (base_mode(MODE) == kPlain) return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 512>(a, c, st);
+            if (c.bwd_threads <= 128) {  // the plain mode's rows of 2 vectors a thread on <= 128 threads
+                if constexpr (base_mode(MODE) == kPlain) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 128>(a, c, st);
                 return cudaErrorInvalidValue;
             }
-            // Only the plain mode runs four vectors on <= 224 threads (the
-            // others take two vectors on up to 512 threads there, run_bwd).
+            return vc ? bwd_t<2, MODE, 256, true>(a, c, st) : bwd_t<2, MODE, 256>(a, c, st);
+        case 4:  // the plain mode only (the others run these rows on two vectors, or on CTA pairs)
             if constexpr (base_mode(MODE) == kPlain) {
-                if (RMSN_BWD_V4_224 && c.bwd_threads <= 224)
+                // Rows of more than 1152 vectors on 512 threads; 4096 < D <= 7168 on <= 224.
+                if (big) return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 512>(a, c, st);
+                if (c.bwd_threads <= 224)
                     return vc ? bwd_t<4, MODE, 224, true>(a, c, st) : bwd_t<4, MODE, 224>(a, c, st);
             }
-            return vc ? cudaErrorInvalidValue : bwd_t<4, MODE, 256>(a, c, st);
+            return cudaErrorInvalidValue;
         default: return cudaErrorInvalidValue;
     }
 }
