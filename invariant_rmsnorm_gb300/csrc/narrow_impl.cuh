@@ -55,6 +55,11 @@ namespace rmsn {
 
 namespace {
 
+// The narrow kernels' 16-byte output stores (y, the copy, dx, dz) at the L2's
+// ordinary write-back policy rather than as streaming (evict-first) stores:
+// Qwen3-Next gated step, 262144 x 128, 91.2 -> 90.7 us.
+__device__ __forceinline__ void st_store_out(void* p, uint4 v) { __stwb(reinterpret_cast<uint4*>(p), v); }
+
 // Device error word of the including translation unit.
 __device__ unsigned int g_narrow_error;
 
@@ -280,9 +285,9 @@ narrow_fwd_kernel(const FwdArgs a, const __grid_constant__ NarrowMaps m, const i
 #pragma unroll
                         for (int e = 0; e < 8; ++e) o[e] = fmul(fmul(f[e], r), we[e]);
                     }
-                    st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(o));
-                    if (M == kResidual) st_global_cs(a.xc + row * a.ldxc + 8 * l, xv);
-                    if (is_fused(MODE)) st_global_cs(a.xc + row * a.ldxc + 8 * l, pack_act<F16>(f));  // x + res
+                    st_store_out(a.y + row * a.ldy + 8 * l, pack_act<F16>(o));
+                    if (M == kResidual) st_store_out(a.xc + row * a.ldxc + 8 * l, xv);
+                    if (is_fused(MODE)) st_store_out(a.xc + row * a.ldxc + 8 * l, pack_act<F16>(f));  // x + res
                 }
             }
         }
@@ -440,8 +445,8 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                         acc[e] = fadd(acc[e], fmul(gf[e], xr));
                         dzv[e] = fmul(gd[e], fmul(xr, we[e]));
                     }
-                    st_global_cs(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
-                    st_global_cs(a.dz + row * a.lddz + 8 * l, pack_act<F16>(dzv));
+                    st_store_out(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
+                    st_store_out(a.dz + row * a.lddz + 8 * l, pack_act<F16>(dzv));
                     if constexpr (RY) {
                         // The forward output again (the forward's operations, same bits).
                         float zf[8], yv[8];
@@ -449,7 +454,7 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
 #pragma unroll
                         for (int e = 0; e < 8; ++e)
                             yv[e] = fmul(fmul(fmul(xf[e], r), we[e]), gate_value<SIG>(zf[e]));
-                        st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
+                        st_store_out(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
                     }
                 } else {
 #pragma unroll
@@ -460,13 +465,13 @@ narrow_bwd_kernel(const BwdArgs a, const __grid_constant__ NarrowMaps m, const i
                         o[e] = d;
                         acc[e] = fadd(acc[e], fmul(fmul(gf[e], xf[e]), r));
                     }
-                    st_global_cs(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
+                    st_store_out(a.dx + row * a.lddx + 8 * l, pack_act<F16>(o));
                     if constexpr (RY) {
                         // The forward output again, from the saved rstd (same bits as the forward).
                         float yv[8];
 #pragma unroll
                         for (int e = 0; e < 8; ++e) yv[e] = fmul(fmul(xf[e], r), we[e]);
-                        st_global_cs(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
+                        st_store_out(a.y + row * a.ldy + 8 * l, pack_act<F16>(yv));
                     }
                 }
             }
