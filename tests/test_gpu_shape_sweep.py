@@ -24,8 +24,9 @@ pytestmark = pytest.mark.gpu
 # Boundaries of the launch shapes (in elements): narrow groups (<= 256), wide
 # VPT 1 (<= 2048 at 256 threads), VPT 2 (<= 4096), VPT 4 on <= 224 threads
 # (<= 7168), then up to 8192 the forward's VPT 4 on 256 threads and the
-# backward's VPT 2 on 512, and VPT 4 on 512 threads beyond.
-BOUNDARY_D = [8, 16, 136, 256, 264, 2048, 2056, 4096, 4104, 7168, 7176, 8192, 8200, 16384]
+# backward's VPT 2 on 512; beyond, the forward's VPT 4 on 512 threads and the
+# backward on CTA pairs (the plain mode up to 9216, then VPT 4 on 512 threads).
+BOUNDARY_D = [8, 16, 136, 256, 264, 2048, 2056, 4096, 4104, 7168, 7176, 8192, 8200, 9216, 9224, 16384]
 
 
 def _draws(n, seed=2024):
