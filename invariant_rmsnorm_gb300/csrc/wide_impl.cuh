@@ -131,8 +131,15 @@ template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_min
 template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_ctas_per_sm() {
     return MAXT == 128 ? 4 : MAXT == 224 ? 2 : VPT == 1 ? RMSN_WIDE_BWD_CTAS_PER_SM_V1 : RMSN_WIDE_BWD_CTAS_PER_SM;
 }
-template <int VPT, int MAXT> __host__ __device__ constexpr int bwd_rows() {
-    return (VPT == 1 && MAXT <= 256) ? RMSN_BWD_ROWS : 1;
+// Rows per backward iteration: RMSN_BWD_ROWS at one vector a thread; two in
+// the plain mode's two-vector kernel on 512 threads (7168 < D <= 8192), which
+// fits them in its 96 registers without spilling (131072 x 8192, backward with
+// pass 2: 1063 -> 996 us); one elsewhere (a second row of three or four
+// operands spills there, and the 256-thread kernels measured mixed).
+template <int VPT, int MAXT, int MODE, bool PAIR = false> __host__ __device__ constexpr int bwd_rows() {
+    return (VPT == 1 && MAXT <= 256)                                       ? RMSN_BWD_ROWS
+           : (VPT == 2 && MAXT > 256 && !PAIR && base_mode(MODE) == kPlain) ? 2
+                                                                            : 1;
 }
 
 constexpr int kConsumerBarrier = 1;  // named barrier id of the consumer warps
@@ -479,7 +486,7 @@ wide_bwd_kernel(const BwdArgs a, const int S) {
     constexpr bool F16 = is_f16(MODE);
     constexpr bool SIG = is_sigmoid_gate(MODE);
     constexpr int NIN = bwd_inputs(MODE);
-    constexpr int R = bwd_rows<VPT, MAXT>();
+    constexpr int R = bwd_rows<VPT, MAXT, MODE, PAIR>();
     constexpr int NWMAX = MAXT / 32;
     constexpr bool RY = is_recompute(MODE);  // also write y (a.y is then not null)
     // Rows per weight-gradient chunk: kWideChunkRows, or with VC the chunk the
@@ -996,7 +1003,7 @@ cudaError_t fwd_t(const FwdArgs& a, const RowCfg& c, cudaStream_t st) {
 template <int VPT, int MODE, int MAXT, bool VC = false, bool PAIR = false>
 cudaError_t bwd_t(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
     constexpr int NIN = bwd_inputs(MODE);
-    constexpr int R = bwd_rows<VPT, MAXT>();
+    constexpr int R = bwd_rows<VPT, MAXT, MODE, PAIR>();
     static_assert(!PAIR || (R == 1 && !VC), "a CTA pair runs one row per iteration in fixed chunks");
     constexpr bool SGS = base_mode(MODE) == kGated && !is_sigmoid_gate(MODE) && VPT <= 2 && RMSN_BWD_LEAN &&
                          RMSN_BWD_SGS;
@@ -1058,7 +1065,13 @@ cudaError_t bwd_dispatch(const BwdArgs& a, const RowCfg& c, cudaStream_t st) {
             // Rows of more than 1024 vectors: a CTA pair per row, two vectors a
             // thread on up to 512 threads in each CTA.
             if (c.bwd_pair) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 512, false, true>(a, c, st);
-            if (big) return vc ? bwd_t<2, MODE, 512, true>(a, c, st) : bwd_t<2, MODE, 512>(a, c, st);
+            if (big) {
+                if (!vc) return bwd_t<2, MODE, 512>(a, c, st);
+                // Shortened chunks on 512 threads: the modes with three or four
+                // operands at 4096 < D <= 7168 (the plain mode runs those on 224).
+                if constexpr (base_mode(MODE) != kPlain) return bwd_t<2, MODE, 512, true>(a, c, st);
+                return cudaErrorInvalidValue;
+            }
             if (c.bwd_threads <= 128) {  // the plain mode's rows of 2 vectors a thread on <= 128 threads
                 if constexpr (base_mode(MODE) == kPlain) return vc ? cudaErrorInvalidValue : bwd_t<2, MODE, 128>(a, c, st);
                 return cudaErrorInvalidValue;
