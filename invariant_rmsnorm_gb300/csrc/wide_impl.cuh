@@ -135,7 +135,10 @@ template <int VPT, int MAXT, int MODE> __host__ __device__ constexpr int bwd_cta
 // the plain mode's two-vector kernel on 512 threads (7168 < D <= 8192), which
 // fits them in its 96 registers without spilling (131072 x 8192, backward with
 // pass 2: 1063 -> 996 us); one elsewhere (a second row of three or four
-// operands spills there, and the 256-thread kernels measured mixed).
+// operands spills there, and the 256-thread kernels measured mixed). An
+// iteration never straddles a chunk, so the rows per iteration divide the
+// 32-row chunk; the stepping kernels, whose shortened chunk can be odd, run
+// at one row (the dispatch gives them no other shape).
 template <int VPT, int MAXT, int MODE, bool PAIR = false> __host__ __device__ constexpr int bwd_rows() {
     return (VPT == 1 && MAXT <= 256)                                       ? RMSN_BWD_ROWS
            : (VPT == 2 && MAXT > 256 && !PAIR && base_mode(MODE) == kPlain) ? 2
